@@ -1,0 +1,128 @@
+"""CPU oracle for the batched symmetric tridiagonal eigensolver.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package entry's ``smoke()``
+check and the benchmark's ``cpu_baseline`` / reference leg may import this
+module.  The CUDA library never links, loads or calls it, and it shares no
+code with the library.
+
+The oracle is plain C (``steqr_oracle.c`` + ``steqr_oracle_impl.h``): implicit
+shifted QL/QR with a Givens bulge chase, one problem at a time, in the
+problem's own precision, following the BatchLAS pages "algo_steqr" (the
+mathematics of steqr) and "perf_steqr" (steqr_cta notes).  This module
+compiles it with gcc (``-O2 -ffp-contract=off``) and wraps it with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_SOURCES = ("steqr_oracle.c", "steqr_oracle_impl.h")
+_lock = threading.Lock()
+_lib = None
+
+DEFAULT_MAXIT_PER_N = 30
+
+
+def build(force: bool = False, src_dir: str = _HERE, out_path: str = _LIB_PATH) -> str:
+    """Compile liboracle.so (idempotent unless a source is newer).  ``src_dir``
+    and ``out_path`` let the tests build a deliberately broken copy."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    srcs = [os.path.join(src_dir, s) for s in _SOURCES]
+    if (not force and os.path.exists(out_path)
+            and all(os.path.getmtime(out_path) >= os.path.getmtime(s) for s in srcs)):
+        return out_path
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+           "-fPIC", "-shared", "-o", tmp, srcs[0], "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True, cwd=src_dir)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _bind(lib):
+    for suffix in ("f32", "f64"):
+        fn = getattr(lib, f"oracle_steqr_batch_{suffix}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_int]
+    lib.oracle_constant.restype = ctypes.c_double
+    lib.oracle_constant.argtypes = [ctypes.c_int, ctypes.c_int]
+    return lib
+
+
+def load_variant(path: str):
+    """Load another build of the oracle (used only by the mutation tests)."""
+    return _bind(ctypes.CDLL(path))
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def constants(dtype) -> dict:
+    """eps, safmin, ssfmax, ssfmin exactly as the oracle uses them."""
+    code = 0 if np.dtype(dtype) == np.float32 else 1
+    lib = _load()
+    return {k: lib.oracle_constant(code, i)
+            for i, k in enumerate(("eps", "safmin", "ssfmax", "ssfmin"))}
+
+
+class Result:
+    """Oracle output for a batch: eigenvalues ``lam`` (batch, n), eigenvectors
+    ``Q`` (batch, n, n) with ``Q[b, :, j]`` the j-th eigenvector (None when
+    jobz = N), ``info`` (batch,) int32 and the summed work counters."""
+
+    def __init__(self, lam, Q, info, sweeps, rotations, solves2x2):
+        self.lam = lam
+        self.Q = Q
+        self.info = info
+        self.sweeps = sweeps
+        self.rotations = rotations
+        self.solves2x2 = solves2x2
+
+
+def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
+          sort: bool = True, nthreads: int = 1, lib=None) -> Result:
+    """Run the oracle on host arrays ``d`` (batch, n) and ``e`` (batch, n-1).
+
+    The dtype of ``d`` (float32 or float64) selects the precision; ``e`` is
+    cast to it.  Inputs are not modified."""
+    d = np.asarray(d)
+    if d.dtype not in (np.float32, np.float64):
+        raise TypeError("oracle: d must be float32 or float64")
+    dt = d.dtype
+    if d.ndim == 1:
+        d = d[None, :]
+    batch, n = d.shape
+    e = np.asarray(e, dtype=dt).reshape(batch, max(n - 1, 0))
+    lam = np.ascontiguousarray(d, dtype=dt).copy()
+    ec = np.ascontiguousarray(e, dtype=dt)
+    Qc = np.empty((batch, n, n), dtype=dt) if jobz else None  # column-major per problem
+    info = np.zeros(batch, dtype=np.int32)
+    cnt = np.zeros(3, dtype=np.int64)
+    lib = lib if lib is not None else _load()
+    fn = lib.oracle_steqr_batch_f32 if dt == np.float32 else lib.oracle_steqr_batch_f64
+    rc = fn(int(n), int(batch), int(bool(jobz)), int(maxit_per_n), int(bool(sort)),
+            lam.ctypes.data, ec.ctypes.data if ec.size else None,
+            Qc.ctypes.data if jobz else None, info.ctypes.data, cnt.ctypes.data,
+            int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle: invalid arguments (n={n}, batch={batch})")
+    Q = None
+    if jobz:
+        # stored column-major per problem: memory [b][j][i] = Q_ij
+        Q = np.ascontiguousarray(np.swapaxes(Qc, 1, 2))
+    return Result(lam, Q, info, int(cnt[0]), int(cnt[1]), int(cnt[2]))

@@ -1,0 +1,103 @@
+"""Seeded synthetic inputs for the batched tridiagonal eigensolver.
+
+This module only draws numbers: it holds none of the solver's arithmetic and
+is shared by the tests, the benchmark and the CPU oracle's callers, so that
+the oracle and the CUDA library consume the very same arrays.
+
+Workload (BatchLAS page "perf_steqr", setup paragraph): random normal d and e.
+Generator: ``numpy.random.default_rng(seed)`` (PCG64); standard normals are
+drawn in float64, in the order d (batch x n), then e (batch x (n-1)), then any
+class extras, and are rounded to the problem's dtype last.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Mixed hard-case batch: class name -> share of the batch.
+MIXED_CLASSES = (
+    ("normal", 0.60),      # d, e i.i.d. N(0,1)
+    ("graded", 0.10),      # d_i = N(0,1) 10^(-i/2), e_i = N(0,1) 10^(-i/2)
+    ("presplit", 0.10),    # each e_i zeroed with probability 1/4, at least one
+    ("zero", 0.05),        # d = e = 0
+    ("big", 0.05),         # N(0,1) scaled by 1e+18
+    ("tiny", 0.05),        # N(0,1) scaled by 1e-18
+    ("toeplitz", 0.05),    # d = a, e = b with a, b ~ N(0,1) per problem
+)
+CLASS_INDEX = {name: i for i, (name, _) in enumerate(MIXED_CLASSES)}
+
+
+def _as_dtype(dtype) -> np.dtype:
+    dt = np.dtype(dtype)
+    if dt not in (np.float32, np.float64):
+        raise TypeError("dtype must be float32 or float64")
+    return dt
+
+
+def normal_problems(n: int, batch: int, dtype, seed: int = 0):
+    """d (batch, n) and e (batch, n-1), i.i.d. N(0,1), rounded to dtype."""
+    dt = _as_dtype(dtype)
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((batch, n))
+    e = rng.standard_normal((batch, max(n - 1, 0)))
+    return d.astype(dt), e.astype(dt)
+
+
+def class_counts(batch: int):
+    """Problems per mixed class; the remainder of the rounding goes to
+    'normal'."""
+    counts = [int(np.floor(batch * share + 1e-9)) for _, share in MIXED_CLASSES]
+    counts[0] += batch - sum(counts)
+    return counts
+
+
+def mixed_problems(n: int, batch: int, dtype, seed: int = 0):
+    """Mixed hard-case batch.  Returns d, e (rounded to dtype), the class label
+    of each problem (int8, index into MIXED_CLASSES) and the Toeplitz (a, b)
+    pair of each problem (float64 before rounding; meaningful only for the
+    'toeplitz' class, whose stored d and e are a and b rounded to dtype)."""
+    dt = _as_dtype(dtype)
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((batch, n))
+    e = rng.standard_normal((batch, max(n - 1, 0)))
+    counts = class_counts(batch)
+    labels = rng.permutation(np.repeat(np.arange(len(MIXED_CLASSES), dtype=np.int8), counts))
+    split_mask = rng.random((batch, max(n - 1, 0))) < 0.25
+    forced = rng.integers(0, max(n - 1, 1), size=batch)
+    ab = rng.standard_normal((batch, 2))
+
+    grade = 10.0 ** (-np.arange(n) / 2.0)
+    g = labels == CLASS_INDEX["graded"]
+    d[g] *= grade[None, :]
+    e[g] *= grade[None, : max(n - 1, 0)]
+
+    p = labels == CLASS_INDEX["presplit"]
+    if n > 1:
+        m = split_mask.copy()
+        m[np.arange(batch), forced] = True
+        e[p] = np.where(m[p], 0.0, e[p])
+
+    z = labels == CLASS_INDEX["zero"]
+    d[z] = 0.0
+    e[z] = 0.0
+
+    b = labels == CLASS_INDEX["big"]
+    d[b] *= 1e18
+    e[b] *= 1e18
+    t = labels == CLASS_INDEX["tiny"]
+    d[t] *= 1e-18
+    e[t] *= 1e-18
+
+    tp = labels == CLASS_INDEX["toeplitz"]
+    d[tp] = ab[tp, 0:1]
+    e[tp] = ab[tp, 1:2]
+    return d.astype(dt), e.astype(dt), labels, ab
+
+
+def problems(kind: str, n: int, batch: int, dtype, seed: int = 0):
+    """``kind`` is 'normal' or 'mixed'; returns (d, e)."""
+    if kind == "normal":
+        return normal_problems(n, batch, dtype, seed)
+    if kind == "mixed":
+        d, e, _, _ = mixed_problems(n, batch, dtype, seed)
+        return d, e
+    raise ValueError(f"unknown input kind {kind!r}")
