@@ -1,0 +1,157 @@
+/*
+ * bstq — batched symmetric tridiagonal eigensolver for one NVIDIA GB300
+ * (sm_103a).  C ABI.
+ *
+ * The operation (BatchLAS page "algo_steqr", problem statement): for each of
+ * `batch` independent matrices T = tridiag(e_1..e_{n-1}; d_1..d_n) compute
+ * T = Q Lambda Q^T with Lambda = diag(lambda_1 <= ... <= lambda_n) and, when
+ * eigenvectors are requested, the orthogonal Q.  The method is implicit
+ * shifted QL/QR with a Givens bulge chase ("steqr"): relative deflation
+ * |e_i|^2 <= eps^2 |d_i||d_{i+1}| + safmin, per-block infinity-norm scaling
+ * against ssfmax/ssfmin, the copysign 2x2 shift, lartg rotations with the
+ * explicit (EXP) similarity update, direct 2x2 solves and a final ascending
+ * sort (all on the "algo_steqr" page; the lane/warp scheduling choices follow
+ * the BatchLAS page "perf_steqr").
+ *
+ * Layout (all arrays dense, row-major over the batch):
+ *   d : batch x n        d[b*n + i]            = d_{i+1} of problem b
+ *   e : batch x (n-1)    e[b*(n-1) + i]        = e_{i+1} of problem b
+ *   Q : batch x n x n    Q[b*n*n + j*n + i]    = Q_{ij}  (column-major per
+ *                        problem; column j is the eigenvector of lambda_j)
+ *
+ * Memory and streams: every pointer of bstq_solve / bstq_solve_ex is caller-
+ * owned DEVICE memory.  The library allocates nothing, never synchronises and
+ * only enqueues work on the given stream; calls are thread-safe.  All
+ * results are valid once the stream reaches them.
+ *
+ * Errors: functions return 0 on success; -k when argument k (1-based) is
+ * invalid; BSTQ_ERR_CUDA (> 0) when a CUDA launch or copy failed (the CUDA
+ * error text is then available from bstq_last_error); BSTQ_ERR_NODEVICE when no
+ * usable sm_103 device is current.  No C++ exception crosses the ABI.
+ * batch == 0 is a no-op returning 0.
+ *
+ * Per-problem status (int32 info[b], first bytes of `work`):
+ *    0  converged;
+ *   k>0 the sweep budget (max_sweeps_per_n * n implicit steps) ran out with
+ *       k off-diagonal entries still nonzero; d and Q hold the current,
+ *       unsorted state of that problem;
+ *   -1  the input had a NaN or Inf; every lambda and every Q entry of that
+ *       problem is NaN.
+ */
+#ifndef BSTQ_H
+#define BSTQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { BSTQ_F32 = 0, BSTQ_F64 = 1 } bstq_dtype;
+typedef enum { BSTQ_JOBZ_N = 0, BSTQ_JOBZ_V = 1 } bstq_jobz;
+
+/* Sweep scheduler within a warp (BatchLAS "perf_steqr", sections "Lockstep
+ * flat solver" and "What ships").  NESTED: each problem runs its own loop
+ * nest.  FLAT: all problems of a warp settle, then chase together.  Both run
+ * the same per-problem operation sequence, so results are equal. */
+typedef enum {
+    BSTQ_SCHED_AUTO = 0,
+    BSTQ_SCHED_FLAT = 1,
+    BSTQ_SCHED_NESTED = 2
+} bstq_scheduler;
+
+/* Where the working copy of Q lives while rotations accumulate. */
+typedef enum {
+    BSTQ_QSTORE_AUTO = 0,
+    BSTQ_QSTORE_REGISTERS = 1, /* whole Q in registers (small n)         */
+    BSTQ_QSTORE_SHARED = 2,    /* per-lane columns in shared memory      */
+    BSTQ_QSTORE_GLOBAL = 3     /* per-lane columns in `work` (L1/L2)     */
+} bstq_qstore;
+
+/* Options; an all-zero struct means the defaults. */
+typedef struct {
+    int no_sort;           /* 0: ascending lambda, Q columns permuted (default)
+                              1: leave eigenpairs in converged order        */
+    int max_sweeps_per_n;  /* 0 -> 30: budget = value * n implicit steps     */
+    int scheduler;         /* bstq_scheduler                                 */
+    int qstore;            /* bstq_qstore                                    */
+    int threads_per_block; /* 0 = chosen by the library; else a multiple of
+                              32 in [32, 1024]                               */
+} bstq_params;
+
+#define BSTQ_ERR_CUDA 1
+#define BSTQ_ERR_NODEVICE 2
+#define BSTQ_MAX_N 32
+
+/* Bytes of device workspace bstq_solve needs for (dtype, jobz, n, batch)
+ * with default parameters: int32 info[batch] at offset 0, then any scratch
+ * the chosen kernel uses (aligned to 256 bytes).  Returns 0 for invalid
+ * arguments. */
+size_t bstq_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch);
+
+/* Same, for explicit parameters (p may be NULL). */
+size_t bstq_work_size_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                         const bstq_params *p);
+
+/*
+ * Solve `batch` problems of size n (1 <= n <= 32) on `stream`
+ * (a cudaStream_t; NULL = legacy default stream).
+ *   d     in/out  batch*n values of dtype; on exit the eigenvalues.
+ *   e     in      batch*(n-1) values; may be NULL when n == 1.
+ *   Q     out     batch*n*n values when jobz == BSTQ_JOBZ_V; ignored (may be
+ *                 NULL) when jobz == BSTQ_JOBZ_N.
+ *   work  in/out  at least bstq_work_size(...) bytes, 16-byte aligned;
+ *                 receives int32 info[batch].
+ * d, e and Q must be aligned to their element size.
+ * Argument numbers for -k: 1 dtype, 2 jobz, 3 n, 4 batch, 5 d, 6 e, 7 Q,
+ * 8 work, 10 params.
+ */
+int bstq_solve(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+               void *d, const void *e, void *Q, void *work, void *stream);
+
+int bstq_solve_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                  void *d, const void *e, void *Q, void *work, void *stream,
+                  const bstq_params *p);
+
+/*
+ * End-to-end variant on HOST buffers: copies h_d and h_e to the device
+ * workspace `dev`, solves there and copies lambda (into h_d), Q (into h_Q,
+ * when jobz == V) and info (into h_info) back, all enqueued on `stream`.
+ * The host buffers are read/written asynchronously when they are pinned
+ * (cudaHostAlloc / cudaHostRegister); the caller synchronises the stream
+ * before reading them.  `dev` must hold bstq_host_work_size(...) bytes of
+ * device memory (256-byte aligned).
+ * Argument numbers for -k: 1 dtype, 2 jobz, 3 n, 4 batch, 5 h_d, 6 h_e,
+ * 7 h_Q, 8 h_info, 9 dev, 11 params.
+ */
+size_t bstq_host_work_size(bstq_dtype dtype, bstq_jobz jobz, int n,
+                           int64_t batch, const bstq_params *p);
+
+int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                    void *h_d, const void *h_e, void *h_Q, int32_t *h_info,
+                    void *dev, void *stream, const bstq_params *p);
+
+/* Description of the kernel the library would launch (for tests and
+ * benchmarks): fills up to `len` bytes of `buf` with a NUL-terminated string
+ * such as "lane<f32,16,V,shared,flat> tpb=224 grid=147" and returns 0, or
+ * returns -k for invalid arguments as bstq_solve_ex would. */
+int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                  const bstq_params *p, char *buf, size_t len);
+
+/* Human-readable text for a return code. */
+const char *bstq_status_string(int code);
+
+/* Library version, e.g. "bstq 0.1.0 sm_103a". */
+const char *bstq_version(void);
+
+/* Text of the last CUDA error a bstq call on this thread returned
+ * BSTQ_ERR_CUDA for ("" if none).  The pointer stays valid until the next
+ * failing call on the same thread. */
+const char *bstq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSTQ_H */

@@ -1,0 +1,191 @@
+"""Thin ctypes binding of libbstq.so (the C ABI in include/bstq.h).
+
+Argument marshalling only: every step of the solve runs in the CUDA library.
+PyTorch supplies device memory and streams.  Importing works without a GPU;
+calling into the library without libbstq.so raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbstq.so")
+
+F32, F64 = 0, 1
+JOBZ_N, JOBZ_V = 0, 1
+SCHED_AUTO, SCHED_FLAT, SCHED_NESTED = 0, 1, 2
+QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL = 0, 1, 2, 3
+ERR_CUDA, ERR_NODEVICE = 1, 2
+MAX_N = 32
+
+# Every symbol include/bstq.h declares.
+EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",
+           "bstq_host_work_size", "bstq_solve_host", "bstq_describe",
+           "bstq_status_string", "bstq_version", "bstq_last_error")
+
+
+class Params(ctypes.Structure):
+    """bstq_params; all-zero means the defaults."""
+    _fields_ = [("no_sort", ctypes.c_int), ("max_sweeps_per_n", ctypes.c_int),
+                ("scheduler", ctypes.c_int), ("qstore", ctypes.c_int),
+                ("threads_per_block", ctypes.c_int)]
+
+
+class BstqError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        extra = ""
+        if code == ERR_CUDA:
+            extra = ": " + load().bstq_last_error().decode()
+        super().__init__(f"{where}: {status_string(code)} (code {code}){extra}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libbstq.so (built by symmetric_tridiagonal_eigensolver_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"libbstq.so not found at {path}; run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        lib = ctypes.CDLL(path)
+        vp, sz, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+        P = ctypes.POINTER(Params)
+        lib.bstq_work_size.restype = sz
+        lib.bstq_work_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64]
+        lib.bstq_work_size_ex.restype = sz
+        lib.bstq_work_size_ex.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P]
+        lib.bstq_solve.restype = ctypes.c_int
+        lib.bstq_solve.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp, vp]
+        lib.bstq_solve_ex.restype = ctypes.c_int
+        lib.bstq_solve_ex.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp, vp, P]
+        lib.bstq_host_work_size.restype = sz
+        lib.bstq_host_work_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P]
+        lib.bstq_solve_host.restype = ctypes.c_int
+        lib.bstq_solve_host.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp,
+                                        vp, vp, P]
+        lib.bstq_describe.restype = ctypes.c_int
+        lib.bstq_describe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P,
+                                      ctypes.c_char_p, sz]
+        lib.bstq_status_string.restype = ctypes.c_char_p
+        lib.bstq_status_string.argtypes = [ctypes.c_int]
+        lib.bstq_version.restype = ctypes.c_char_p
+        lib.bstq_version.argtypes = []
+        lib.bstq_last_error.restype = ctypes.c_char_p
+        lib.bstq_last_error.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0):
+    return Params(int(bool(no_sort)), int(max_sweeps_per_n), int(scheduler), int(qstore),
+                  int(threads_per_block))
+
+
+def _dtype_code(dt) -> int:
+    import torch
+    if dt in (torch.float32, np.float32):
+        return F32
+    if dt in (torch.float64, np.float64):
+        return F64
+    raise TypeError(f"bstq: dtype must be float32 or float64, got {dt}")
+
+
+def status_string(code: int) -> str:
+    return load().bstq_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return load().bstq_version().decode()
+
+
+def work_size(dtype, jobz: bool, n: int, batch: int, **params) -> int:
+    code = _dtype_code(dtype)
+    p = _params(**params)
+    return int(load().bstq_work_size_ex(code, int(bool(jobz)), int(n), int(batch), ctypes.byref(p)))
+
+
+def describe(dtype, jobz: bool, n: int, batch: int, **params) -> str:
+    p = _params(**params)
+    buf = ctypes.create_string_buffer(256)
+    rc = load().bstq_describe(_dtype_code(dtype), int(bool(jobz)), int(n), int(batch),
+                              ctypes.byref(p), buf, 256)
+    if rc != 0:
+        raise BstqError(rc, "bstq_describe")
+    return buf.value.decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def solve(d, e, jobz: bool = True, Q=None, work=None, stream=None, **params):
+    """Solve on CUDA tensors: ``d`` (batch, n) in/out (eigenvalues on exit),
+    ``e`` (batch, n-1).  Returns (d, Q, info) where Q is (batch, n, n) with
+    Q[b, :, j] the eigenvector of d[b, j] (None for jobz N) and info (batch,)
+    int32.  Work is enqueued on ``stream`` (default: torch's current stream);
+    nothing is synchronised."""
+    import torch
+    if not (d.is_cuda and d.is_contiguous()):
+        raise ValueError("bstq.solve: d must be a contiguous CUDA tensor")
+    if d.dim() != 2:
+        raise ValueError("bstq.solve: d must be (batch, n)")
+    batch, n = d.shape
+    code = _dtype_code(d.dtype)
+    if e is None or e.numel() == 0:
+        e_ptr = None
+    else:
+        if not (e.is_cuda and e.is_contiguous() and e.dtype == d.dtype and e.numel() == batch * (n - 1)):
+            raise ValueError("bstq.solve: e must be a contiguous CUDA tensor of d's dtype, (batch, n-1)")
+        e_ptr = e.data_ptr()
+    p = _params(**params)
+    lib = load()
+    wbytes = int(lib.bstq_work_size_ex(code, int(bool(jobz)), int(n), int(batch), ctypes.byref(p)))
+    if wbytes == 0:
+        raise BstqError(-10, "bstq_work_size_ex")
+    if work is None:
+        work = torch.empty(wbytes, dtype=torch.uint8, device=d.device)
+    elif work.numel() * work.element_size() < wbytes:
+        raise ValueError(f"bstq.solve: work needs {wbytes} bytes")
+    if jobz and Q is None:
+        Q = torch.empty((batch, n, n), dtype=d.dtype, device=d.device)
+    # the library writes column-major per problem: memory [b][j][i] = Q_ij
+    rc = lib.bstq_solve_ex(code, int(bool(jobz)), int(n), int(batch), d.data_ptr(), e_ptr,
+                           Q.data_ptr() if jobz else None, work.data_ptr(), _stream_handle(stream),
+                           ctypes.byref(p))
+    if rc != 0:
+        raise BstqError(rc, "bstq_solve_ex")
+    info = work[: 4 * batch].view(torch.int32)
+    Qout = Q.transpose(1, 2) if jobz else None
+    return d, Qout, info
+
+
+def host_work_size(dtype, jobz: bool, n: int, batch: int, **params) -> int:
+    p = _params(**params)
+    return int(load().bstq_host_work_size(_dtype_code(dtype), int(bool(jobz)), int(n), int(batch),
+                                          ctypes.byref(p)))
+
+
+def solve_host(h_d, h_e, h_Q, h_info, dev, stream=None, jobz: bool = True, **params):
+    """End-to-end call on host buffers (pinned torch CPU tensors): copies in,
+    solves and copies out on ``stream``; the caller synchronises."""
+    batch, n = h_d.shape
+    p = _params(**params)
+    rc = load().bstq_solve_host(_dtype_code(h_d.dtype), int(bool(jobz)), int(n), int(batch),
+                                h_d.data_ptr(), h_e.data_ptr() if h_e is not None and h_e.numel() else None,
+                                h_Q.data_ptr() if jobz else None, h_info.data_ptr(), dev.data_ptr(),
+                                _stream_handle(stream), ctypes.byref(p))
+    if rc != 0:
+        raise BstqError(rc, "bstq_solve_host")

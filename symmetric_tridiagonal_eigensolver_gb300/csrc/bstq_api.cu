@@ -1,0 +1,402 @@
+// C ABI of the batched tridiagonal eigensolver: argument checks, the launch
+// plan (kernel variant, block size, grid, workspace) and the launches.
+#include <cuda_runtime.h>
+
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/bstq.h"
+#include "bstq_lane.cuh"
+#include "bstq_registry.h"
+
+namespace bstq {
+namespace {
+
+struct Plan {
+    const KernelEntry *k = nullptr;
+    int tpb = 0;
+    long long grid = 0;
+    size_t smem = 0;
+    size_t qwork_bytes = 0;
+    size_t work_bytes = 0;
+};
+
+constexpr int kNmList[] = {4, 8, 12, 16, 24, 32};
+
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t err, const char *what)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorString(err),
+             cudaGetErrorName(err));
+    return BSTQ_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct DevInfo {
+    int sms = 0;
+    int max_smem_block = 0;
+    int max_regs_sm = 0;
+    int max_threads_sm = 0;
+    int major = 0, minor = 0;
+};
+
+// Device properties of the current device, cached per device ordinal.
+bool dev_info(DevInfo &out)
+{
+    static std::mutex mu;
+    static DevInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DevInfo di;
+        if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        cache[dev] = di;
+        have[dev] = true;
+    }
+    out = cache[dev];
+    return true;
+}
+
+const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched)
+{
+    typedef const KernelEntry *(*Lister)(int *);
+#define BSTQ_LISTER(name) entries_##name,
+    static const Lister lists[] = {BSTQ_FOR_EACH_UNIT(BSTQ_LISTER)};
+#undef BSTQ_LISTER
+    for (Lister l : lists) {
+        int cnt = 0;
+        const KernelEntry *t = l(&cnt);
+        for (int i = 0; i < cnt; ++i)
+            if (t[i].dtype == dtype && t[i].jobz == jobz && t[i].nm == nm &&
+                t[i].qs == (jobz ? qs : 0) && t[i].sched == sched)
+                return &t[i];
+    }
+    return nullptr;
+}
+
+// Default Q storage: registers while a whole Q fits comfortably, then shared
+// memory for float (n <= 16 keeps one wave of 32768 problems resident), and
+// global scratch otherwise (float64 is bound by its FP64 pipe, not by L2).
+int default_qstore(int dtype, int nm)
+{
+    if (dtype == 0)
+        return nm <= 12 ? QS_REG : QS_SMEM;
+    return nm <= 8 ? QS_REG : QS_GLOBAL;
+}
+
+// Default scheduler per (dtype, chunk): flat lockstep.
+int default_sched(int, int) { return SCHED_FLAT; }
+
+int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p)
+{
+    if (dtype != BSTQ_F32 && dtype != BSTQ_F64)
+        return -1;
+    if (jobz != BSTQ_JOBZ_N && jobz != BSTQ_JOBZ_V)
+        return -2;
+    if (n < 1 || n > BSTQ_MAX_N)
+        return -3;
+    if (batch < 0)
+        return -4;
+    if (p) {
+        if (p->no_sort != 0 && p->no_sort != 1)
+            return -10;
+        if (p->max_sweeps_per_n < 0 || p->max_sweeps_per_n > 1000000)
+            return -10;
+        if (p->scheduler < 0 || p->scheduler > 2)
+            return -10;
+        if (p->qstore < 0 || p->qstore > 3)
+            return -10;
+        if (p->threads_per_block != 0 &&
+            (p->threads_per_block < 32 || p->threads_per_block > 1024 || p->threads_per_block % 32))
+            return -10;
+    }
+    return 0;
+}
+
+// Build the launch plan.  Returns 0, -10 for parameters no kernel supports,
+// or BSTQ_ERR_NODEVICE.
+int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p, Plan &pl)
+{
+    DevInfo di;
+    if (!dev_info(di))
+        return BSTQ_ERR_NODEVICE;
+    int nm = 0;
+    for (int v : kNmList)
+        if (v >= n) {
+            nm = v;
+            break;
+        }
+    const int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm)) : 0;
+    const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
+    pl.k = find_entry(dtype, jobz, nm, qs, sched);
+    if (!pl.k)
+        return -10;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, pl.k->fn) != cudaSuccess) {
+        cudaGetLastError();
+        return BSTQ_ERR_NODEVICE;
+    }
+    const size_t elem = dtype ? 8 : 4;
+    const int groups = (int)((nm * elem + 15) / 16);
+    const size_t smem_per_thread = (qs == QS_SMEM) ? size_t(nm) * groups * 16 : 0;
+    // Threads an SM can hold for this kernel.
+    const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
+    int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);
+    cap = cap / 32 * 32;
+    if (cap > di.max_threads_sm)
+        cap = di.max_threads_sm;
+    if (smem_per_thread) {
+        const int by_smem = (int)((size_t)di.max_smem_block / smem_per_thread) / 32 * 32;
+        if (by_smem < cap)
+            cap = by_smem;
+    }
+    if (cap > fa.maxThreadsPerBlock)
+        cap = fa.maxThreadsPerBlock / 32 * 32;
+    if (cap > 1024)
+        cap = 1024;
+    if (cap < 32)
+        return -10;
+    int tpb;
+    if (p && p->threads_per_block) {
+        tpb = p->threads_per_block;
+        if (tpb > cap)
+            return -10;
+    } else {
+        // One wave of one block per SM when the whole batch fits, so the
+        // problems spread evenly over all SMs; otherwise 128-thread blocks.
+        const long long want = (batch + di.sms - 1) / di.sms;
+        if (want <= cap) {
+            tpb = (int)((want + 31) / 32 * 32);
+            if (tpb < 32)
+                tpb = 32;
+        } else {
+            tpb = cap < 128 ? cap : 128;
+        }
+    }
+    pl.tpb = tpb;
+    pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
+    pl.smem = smem_per_thread * tpb;
+    pl.qwork_bytes = (qs == QS_GLOBAL) ? size_t(pl.grid) * nm * groups * 16 * tpb : 0;
+    pl.work_bytes = align256(size_t(batch) * 4) + pl.qwork_bytes;
+    if (pl.work_bytes == 0)
+        pl.work_bytes = 256;
+    return 0;
+}
+
+const char *qs_name(int qs)
+{
+    switch (qs) {
+    case QS_REG: return "registers";
+    case QS_SMEM: return "shared";
+    case QS_GLOBAL: return "global";
+    default: return "none";
+    }
+}
+
+int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const void *e, void *Q,
+           void *work, cudaStream_t st, const bstq_params *p)
+{
+    KParams kp;
+    kp.d = d;
+    kp.e = e;
+    kp.Q = Q;
+    kp.info = reinterpret_cast<int *>(work);
+    kp.qwork = pl.qwork_bytes ? reinterpret_cast<char *>(work) + align256(size_t(batch) * 4) : nullptr;
+    kp.batch = batch;
+    kp.n = n;
+    const int per_n = (p && p->max_sweeps_per_n) ? p->max_sweeps_per_n : 30;
+    kp.budget = per_n * n;
+    kp.sort = (p && p->no_sort) ? 0 : 1;
+    (void)dtype;
+    if (pl.smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "cudaFuncSetAttribute");
+    }
+    void *args[] = {&kp};
+    if (pl.grid > 0x7fffffffLL)
+        return -4;
+    cudaError_t err = cudaLaunchKernel(pl.k->fn, dim3((unsigned)pl.grid), dim3(pl.tpb), args, pl.smem, st);
+    return err == cudaSuccess ? 0 : cuda_fail(err, "cudaLaunchKernel");
+}
+
+bool misaligned(const void *ptr, size_t a) { return ptr && (reinterpret_cast<uintptr_t>(ptr) % a) != 0; }
+
+}  // namespace
+}  // namespace bstq
+
+using namespace bstq;
+
+extern "C" size_t bstq_work_size_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                                    const bstq_params *p)
+{
+    if (check_args(dtype, jobz, n, batch, p) != 0)
+        return 0;
+    Plan pl;
+    if (make_plan(dtype, jobz, n, batch, p, pl) != 0)
+        return 0;
+    return pl.work_bytes;
+}
+
+extern "C" size_t bstq_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch)
+{
+    return bstq_work_size_ex(dtype, jobz, n, batch, nullptr);
+}
+
+extern "C" int bstq_solve_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, void *d,
+                             const void *e, void *Q, void *work, void *stream, const bstq_params *p)
+{
+    int rc = check_args(dtype, jobz, n, batch, p);
+    if (rc)
+        return rc;
+    if (batch == 0)
+        return 0;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    if (!d || misaligned(d, elem))
+        return -5;
+    if ((n > 1 && !e) || misaligned(e, elem))
+        return -6;
+    if (jobz == BSTQ_JOBZ_V && (!Q || misaligned(Q, elem)))
+        return -7;
+    if (!work || misaligned(work, 16))
+        return -8;
+    Plan pl;
+    rc = make_plan(dtype, jobz, n, batch, p, pl);
+    if (rc)
+        return rc;
+    return launch(pl, n, batch, dtype, d, e, Q, work, reinterpret_cast<cudaStream_t>(stream), p);
+}
+
+extern "C" int bstq_solve(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, void *d, const void *e,
+                          void *Q, void *work, void *stream)
+{
+    return bstq_solve_ex(dtype, jobz, n, batch, d, e, Q, work, stream, nullptr);
+}
+
+// Device workspace layout of bstq_solve_host: d | e | Q | work, each 256-byte
+// aligned.
+extern "C" size_t bstq_host_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                                      const bstq_params *p)
+{
+    if (check_args(dtype, jobz, n, batch, p) != 0)
+        return 0;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    size_t w = bstq_work_size_ex(dtype, jobz, n, batch, p);
+    if (w == 0)
+        return 0;
+    size_t total = align256(elem * n * batch) + align256(elem * (n > 1 ? n - 1 : 1) * batch) +
+                   (jobz == BSTQ_JOBZ_V ? align256(elem * n * n * batch) : 0) + w;
+    return total;
+}
+
+extern "C" int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, void *h_d,
+                               const void *h_e, void *h_Q, int32_t *h_info, void *dev, void *stream,
+                               const bstq_params *p)
+{
+    int rc = check_args(dtype, jobz, n, batch, p);
+    if (rc)
+        return rc == -10 ? -11 : rc;
+    if (batch == 0)
+        return 0;
+    if (!h_d)
+        return -5;
+    if (n > 1 && !h_e)
+        return -6;
+    if (jobz == BSTQ_JOBZ_V && !h_Q)
+        return -7;
+    if (!h_info)
+        return -8;
+    if (!dev || misaligned(dev, 256))
+        return -9;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    char *base = reinterpret_cast<char *>(dev);
+    const size_t bd = elem * n * batch, be = elem * (n > 1 ? n - 1 : 0) * batch;
+    const size_t bq = jobz == BSTQ_JOBZ_V ? elem * n * n * batch : 0;
+    char *dd = base;
+    char *de = dd + align256(bd);
+    char *dq = de + align256(be > 0 ? be : elem * batch);
+    char *dw = dq + (bq ? align256(bq) : 0);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if ((err = cudaMemcpyAsync(dd, h_d, bd, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync d");
+    if (be && (err = cudaMemcpyAsync(de, h_e, be, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync e");
+    rc = bstq_solve_ex(dtype, jobz, n, batch, dd, de, bq ? dq : nullptr, dw, stream, p);
+    if (rc)
+        return rc == -10 ? -11 : (rc < 0 ? -9 : rc);
+    if ((err = cudaMemcpyAsync(h_d, dd, bd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync lambda");
+    if (bq && (err = cudaMemcpyAsync(h_Q, dq, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync Q");
+    if ((err = cudaMemcpyAsync(h_info, dw, 4 * size_t(batch), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync info");
+    return 0;
+}
+
+extern "C" int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const bstq_params *p,
+                             char *buf, size_t len)
+{
+    int rc = check_args(dtype, jobz, n, batch, p);
+    if (rc)
+        return rc;
+    Plan pl;
+    rc = make_plan(dtype, jobz, n, batch, p, pl);
+    if (rc)
+        return rc;
+    if (buf && len) {
+        cudaFuncAttributes fa;
+        int regs = 0;
+        if (cudaFuncGetAttributes(&fa, pl.k->fn) == cudaSuccess)
+            regs = fa.numRegs;
+        else
+            cudaGetLastError();
+        snprintf(buf, len, "lane<%s,%d,%s,%s,%s> tpb=%d grid=%lld smem=%zu regs=%d work=%zu",
+                 dtype ? "f64" : "f32", pl.k->nm, jobz ? "V" : "N", jobz ? qs_name(pl.k->qs) : "none",
+                 pl.k->sched == SCHED_FLAT ? "flat" : "nested", pl.tpb, pl.grid, pl.smem, regs, pl.work_bytes);
+    }
+    return 0;
+}
+
+extern "C" const char *bstq_status_string(int code)
+{
+    switch (code) {
+    case 0: return "success";
+    case BSTQ_ERR_CUDA: return "CUDA launch or copy failed";
+    case BSTQ_ERR_NODEVICE: return "no usable CUDA device is current";
+    case -1: return "invalid dtype";
+    case -2: return "invalid jobz";
+    case -3: return "n outside [1, 32]";
+    case -4: return "invalid batch";
+    case -5: return "d is NULL or misaligned";
+    case -6: return "e is NULL or misaligned";
+    case -7: return "Q is NULL or misaligned";
+    case -8: return "work is NULL, misaligned or info buffer missing";
+    case -9: return "invalid device workspace";
+    case -10: return "invalid or unsupported parameters";
+    case -11: return "invalid or unsupported parameters";
+    default: return "unknown status";
+    }
+}
+
+extern "C" const char *bstq_version(void) { return "bstq 0.1.0 sm_103a"; }
+
+extern "C" const char *bstq_last_error(void) { return g_last_error; }

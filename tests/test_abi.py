@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every symbol include/bstq.h declares and
+rejects invalid arguments with the documented codes (CPU only: no compute
+call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from symmetric_tridiagonal_eigensolver_gb300 import bstq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bstq.LIB_PATH):
+        from symmetric_tridiagonal_eigensolver_gb300 import build
+        build.build()
+    return bstq.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bstq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bstq_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(bstq.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert bstq.version().startswith("bstq")
+    assert bstq.status_string(0) == "success"
+    assert "n outside" in bstq.status_string(-3)
+
+
+def test_invalid_arguments_are_rejected_before_any_device_use(lib):
+    vp = ctypes.c_void_p
+    buf = (ctypes.c_char * 64)()
+    good = ctypes.cast(buf, vp)
+    solve = lib.bstq_solve
+    assert solve(7, 1, 8, 10, good, good, good, good, None) == -1
+    assert solve(0, 5, 8, 10, good, good, good, good, None) == -2
+    assert solve(0, 1, 0, 10, good, good, good, good, None) == -3
+    assert solve(0, 1, 33, 10, good, good, good, good, None) == -3
+    assert solve(0, 1, 8, -1, good, good, good, good, None) == -4
+    assert solve(0, 1, 8, 0, None, None, None, None, None) == 0   # batch 0: no-op
+    assert solve(0, 1, 8, 10, None, good, good, good, None) == -5
+    assert solve(0, 1, 8, 10, good, None, good, good, None) == -6
+    assert solve(0, 1, 8, 10, good, good, None, good, None) == -7
+    assert solve(0, 1, 8, 10, good, good, good, None, None) == -8
+    mis = ctypes.c_void_p(ctypes.addressof(buf) + 2)
+    assert solve(0, 1, 8, 10, mis, good, good, good, None) == -5
+    p = bstq.Params(0, 0, 9, 0, 0)
+    assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
+    p = bstq.Params(0, 0, 0, 0, 48)
+    assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
+    assert lib.bstq_work_size(0, 1, 40, 10) == 0
+    assert lib.bstq_solve_host(0, 1, 8, 10, None, good, good, good, good, None, None) == -5
+
+
+def test_no_device_is_reported_not_faked(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    vp = ctypes.c_void_p
+    buf = (ctypes.c_char * 64)()
+    good = ctypes.cast(buf, vp)
+    rc = lib.bstq_solve(0, 1, 8, 10, good, good, good, good, None)
+    assert rc == bstq.ERR_NODEVICE
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The library and its binding never import or load the oracle."""
+    pkg = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "liboracle" not in text, f

@@ -1,0 +1,91 @@
+"""Kernel variants (schedulers, Q storage, block sizes, streams, the host
+entry point) must agree with one another and with the oracle."""
+import numpy as np
+import pytest
+
+from symmetric_tridiagonal_eigensolver_gb300 import inputs
+from tests.gpu_helpers import check_parity, oracle_ref, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dt,n", [(np.float32, 4), (np.float32, 8), (np.float32, 12), (np.float32, 16),
+                                  (np.float32, 24), (np.float32, 32), (np.float64, 4), (np.float64, 8),
+                                  (np.float64, 12), (np.float64, 16), (np.float64, 24), (np.float64, 32)])
+@pytest.mark.parametrize("jobz", [True, False])
+def test_flat_equals_nested(dt, n, jobz):
+    """The flat lockstep and the nested scheduler run the same per-problem
+    operations, so their results are equal (perf_steqr, Lockstep flat
+    solver: bitwise equal on the dump cases)."""
+    d, e, _, _ = inputs.mixed_problems(n, 4096, dt, seed=n)
+    a = run_gpu(d, e, jobz=jobz, scheduler=1)
+    b = run_gpu(d, e, jobz=jobz, scheduler=2)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[2], b[2])
+    if jobz:
+        np.testing.assert_array_equal(a[1], b[1])
+    check_parity(d, e, *a, oracle_ref(d, e, jobz=jobz), what=f"flat {n}")
+
+
+@pytest.mark.parametrize("dt,n,qs", [(np.float32, 16, 3), (np.float32, 24, 3), (np.float64, 12, 2),
+                                     (np.float64, 12, 3), (np.float64, 16, 3)])
+def test_qstore_variants_agree(dt, n, qs):
+    d, e = inputs.normal_problems(n, 5000, dt, seed=7)
+    ref = oracle_ref(d, e)
+    a = run_gpu(d, e, qstore=qs)
+    check_parity(d, e, *a, ref, what=f"qstore={qs}")
+    b = run_gpu(d, e)
+    np.testing.assert_array_equal(a[0], b[0])
+
+
+@pytest.mark.parametrize("tpb", [32, 64, 96, 224])
+def test_block_size_does_not_change_results(tpb):
+    """Block size changes the launch shape only (perf_steqr, Work-group
+    multiplier: byte-identical outputs)."""
+    d, e = inputs.normal_problems(16, 3000, np.float32, seed=8)
+    a = run_gpu(d, e, threads_per_block=tpb)
+    b = run_gpu(d, e)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_host_entry_point_matches_device_path():
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    n, batch = 12, 2000
+    d, e = inputs.normal_problems(n, batch, np.float64, seed=9)
+    hd = torch.from_numpy(d.copy()).pin_memory()
+    he = torch.from_numpy(e.copy()).pin_memory()
+    hq = torch.empty((batch, n, n), dtype=torch.float64).pin_memory()
+    hi = torch.empty(batch, dtype=torch.int32).pin_memory()
+    dev = torch.empty(bstq.host_work_size(np.float64, True, n, batch), dtype=torch.uint8, device="cuda")
+    bstq.solve_host(hd, he, hq, hi, dev, jobz=True)
+    torch.cuda.synchronize()
+    lam, Q, info = run_gpu(d, e)
+    np.testing.assert_array_equal(hd.numpy(), lam)
+    np.testing.assert_array_equal(hq.numpy().transpose(0, 2, 1), Q)
+    np.testing.assert_array_equal(hi.numpy(), info)
+
+
+def test_streams_are_honoured():
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    n, batch = 16, 8192
+    d, e = inputs.normal_problems(n, batch, np.float32, seed=10)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for s in (s1, s2):
+        with torch.cuda.stream(s):
+            dg = torch.from_numpy(d.copy()).cuda()
+            eg = torch.from_numpy(e.copy()).cuda()
+            outs.append(bstq.solve(dg, eg, jobz=True, stream=s))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(outs[0][0].cpu().numpy(), outs[1][0].cpu().numpy())
+
+
+def test_oversized_block_is_rejected_not_launched():
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    # 256 threads x 1 KiB of shared Q exceeds what one block may hold
+    with pytest.raises(bstq.BstqError) as ei:
+        run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), threads_per_block=1024)
+    assert ei.value.code == -10
