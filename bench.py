@@ -136,7 +136,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def time_workload(w, steps, warmup, dist_barrier, flush, stream):
+def time_workload(w, steps, warmup, dist_barrier, flush, stream, **params):
     """Device-side timing of `steps` solves; returns (ms list, counts, extra)."""
     import torch
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
@@ -147,8 +147,9 @@ def time_workload(w, steps, warmup, dist_barrier, flush, stream):
     eg = torch.from_numpy(e).to(dev)
     dg = torch.empty_like(d0)
     Q = torch.empty((w["batch"], w["n"], w["n"]), dtype=d0.dtype, device=dev) if w["jobz"] else None
-    work = torch.empty(bstq.work_size(dt, w["jobz"], w["n"], w["batch"]), dtype=torch.uint8, device=dev)
-    desc = bstq.describe(dt, w["jobz"], w["n"], w["batch"])
+    work = torch.empty(bstq.work_size(dt, w["jobz"], w["n"], w["batch"], **params), dtype=torch.uint8,
+                       device=dev)
+    desc = bstq.describe(dt, w["jobz"], w["n"], w["batch"], **params)
     times = []
     with torch.cuda.stream(stream):
         for it in range(warmup + steps):
@@ -159,7 +160,7 @@ def time_workload(w, steps, warmup, dist_barrier, flush, stream):
                 torch.cuda.synchronize()
             s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
-            bstq.solve(dg, eg, jobz=w["jobz"], Q=Q, work=work, stream=stream)
+            bstq.solve(dg, eg, jobz=w["jobz"], Q=Q, work=work, stream=stream, **params)
             t.record(stream)
             if it >= warmup:
                 times.append((s, t))
@@ -264,6 +265,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-companions", action="store_true")
+    ap.add_argument("--sched", type=int, default=0, help="0 auto, 1 flat, 2 nested (with --only)")
+    ap.add_argument("--qstore", type=int, default=0, help="Q storage policy (with --only)")
     ap.add_argument("--only", default=None,
                     help="time one workload 'dtype:n:V|N[:batch]' and print its line (profiling aid)")
     args = ap.parse_args()
@@ -303,7 +306,8 @@ def main():
         parts = args.only.split(":")
         w = dict(dtype={"f32": "float32", "f64": "float64"}.get(parts[0], parts[0]), n=int(parts[1]),
                  jobz=parts[2].upper() == "V", batch=int(parts[3]) if len(parts) > 3 else 32768)
-        wm, wd, we, wdesc = time_workload(w, args.steps, args.warmup, barrier, flush, stream)
+        wm, wd, we, wdesc = time_workload(w, args.steps, args.warmup, barrier, flush, stream,
+                                          scheduler=args.sched, qstore=args.qstore)
         t = statistics.mean(wm) / 1e3
         print(json.dumps({"workload": wl_name(w), "ms": t * 1e3, "problems_per_s": w["batch"] / t,
                           "kernel": wdesc}))

@@ -66,7 +66,8 @@ typedef enum {
     BSTQ_QSTORE_AUTO = 0,
     BSTQ_QSTORE_REGISTERS = 1, /* whole Q in registers (small n)         */
     BSTQ_QSTORE_SHARED = 2,    /* per-lane columns in shared memory      */
-    BSTQ_QSTORE_GLOBAL = 3     /* per-lane columns in `work` (L1/L2)     */
+    BSTQ_QSTORE_GLOBAL = 3,    /* per-lane columns in `work` (L1/L2)     */
+    BSTQ_QSTORE_HYBRID = 4     /* 8 rows in registers, rest in shared    */
 } bstq_qstore;
 
 /* Options; an all-zero struct means the defaults. */

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libbstq.so")
 F32, F64 = 0, 1
 JOBZ_N, JOBZ_V = 0, 1
 SCHED_AUTO, SCHED_FLAT, SCHED_NESTED = 0, 1, 2
-QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL = 0, 1, 2, 3
+QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID = 0, 1, 2, 3, 4
 ERR_CUDA, ERR_NODEVICE = 1, 2
 MAX_N = 32
 

@@ -92,14 +92,25 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched)
     return nullptr;
 }
 
-// Default Q storage: registers while a whole Q fits comfortably, then shared
-// memory for float (n <= 16 keeps one wave of 32768 problems resident), and
-// global scratch otherwise (float64 is bound by its FP64 pipe, not by L2).
+// Default Q storage: registers while a whole Q fits (n <= 12 in float,
+// n <= 8 in double); float n >= 16 keeps 8 rows of Q in registers and
+// streams the rest from shared memory (one wave of 32768 problems stays
+// resident); double streams Q from global scratch (its FP64 pipe, not L1/L2,
+// bounds it).
 int default_qstore(int dtype, int nm)
 {
     if (dtype == 0)
-        return nm <= 12 ? QS_REG : QS_SMEM;
+        return nm <= 12 ? QS_REG : QS_HYBRID;
     return nm <= 8 ? QS_REG : QS_GLOBAL;
+}
+
+// Rows of Q held in memory per lane (registers hold the rest), padded to
+// whole 16-byte vectors.
+int memory_rows(int dtype, int nm, int qs)
+{
+    const int w = dtype ? 2 : 4;
+    const int rr = qs == QS_REG ? nm : (qs == QS_HYBRID ? kHybridRegRows : 0);
+    return qs == QS_REG ? 0 : ((nm - rr + w - 1) / w) * w;
 }
 
 // Default scheduler per (dtype, chunk): flat lockstep.
@@ -122,7 +133,7 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
             return -10;
         if (p->scheduler < 0 || p->scheduler > 2)
             return -10;
-        if (p->qstore < 0 || p->qstore > 3)
+        if (p->qstore < 0 || p->qstore > 4)
             return -10;
         if (p->threads_per_block != 0 &&
             (p->threads_per_block < 32 || p->threads_per_block > 1024 || p->threads_per_block % 32))
@@ -155,8 +166,11 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         return BSTQ_ERR_NODEVICE;
     }
     const size_t elem = dtype ? 8 : 4;
-    const int groups = (int)((nm * elem + 15) / 16);
-    const size_t smem_per_thread = (qs == QS_SMEM) ? size_t(nm) * groups * 16 : 0;
+    const size_t mem_per_thread = jobz ? size_t(nm) * memory_rows(dtype, nm, qs) * elem : 0;
+    // shared memory per thread: the memory rows of Q (shared / hybrid) and
+    // the mirror of d and e the settle step reads at dynamic positions
+    const size_t smem_per_thread =
+        ((qs == QS_SMEM || qs == QS_HYBRID) ? mem_per_thread : 0) + 2 * size_t(nm) * elem;
     // Threads an SM can hold for this kernel.
     const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
     int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);
@@ -194,7 +208,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     pl.tpb = tpb;
     pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
     pl.smem = smem_per_thread * tpb;
-    pl.qwork_bytes = (qs == QS_GLOBAL) ? size_t(pl.grid) * nm * groups * 16 * tpb : 0;
+    pl.qwork_bytes = (qs == QS_GLOBAL) ? size_t(pl.grid) * mem_per_thread * tpb : 0;
     pl.work_bytes = align256(size_t(batch) * 4) + pl.qwork_bytes;
     if (pl.work_bytes == 0)
         pl.work_bytes = 256;
@@ -207,6 +221,7 @@ const char *qs_name(int qs)
     case QS_REG: return "registers";
     case QS_SMEM: return "shared";
     case QS_GLOBAL: return "global";
+    case QS_HYBRID: return "hybrid";
     default: return "none";
     }
 }

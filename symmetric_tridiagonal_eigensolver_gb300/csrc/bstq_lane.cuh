@@ -1,11 +1,15 @@
 // Lane-per-problem steqr kernel for sm_103a.
 //
 // One CUDA thread owns one tridiagonal problem of size n <= NM.  d and e live
-// in registers and every access uses a compile-time index: the bulge chase is
-// unrolled over the static positions NM-1 .. 1 and the warp skips positions
-// outside the union of its lanes' active ranges.  Dynamic positions (the
-// start of a sweep, the deflation point) only occur in the settle step and
-// are resolved with bit masks and select chains.
+// in registers and every access uses a compile-time index: a sweep is a pass
+// over the static chase positions C = NM-1 .. 1, entered through a jump table
+// at the warp's highest active position and left at a group boundary once no
+// lane has work below.  Each position is straight-line code: lanes for which
+// the position is outside their sweep apply the identity rotation (lartg of
+// (1, 0)) and keep d and e through selects, so a whole pass is one basic block
+// in which the eigenvector update of one position overlaps the dependency
+// chain of the next.  Dynamic positions (start of a sweep, deflation point)
+// only occur in the settle step and are resolved with bit masks and selects.
 //
 // QR runs as QL on the mirrored block (BatchLAS page "perf_steqr", section
 // "CTA STEQR: chase micro-structure decisions"; page "algo_steqr", QL on
@@ -28,19 +32,20 @@
 
 namespace bstq {
 
-enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3 };
+enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3, QS_HYBRID = 4 };
 enum { SCHED_FLAT = 1, SCHED_NESTED = 2 };
 enum { ST_RUN = 0, ST_DONE = 1, ST_FAIL = 2, ST_BAD = 3, ST_DEAD = 4 };
 enum { TASK_NONE = 0, TASK_SWEEP = 1, TASK_2X2 = 2 };
 
 constexpr unsigned FULL = 0xffffffffu;
+constexpr int kHybridRegRows = 8;
 
 struct KParams {
     void *d;           // batch x n, in/out
     const void *e;     // batch x (n-1)
     void *Q;           // batch x n x n (column-major per problem), out
     int *info;         // batch
-    void *qwork;       // scratch for QS_GLOBAL: gridDim.x * NM * G * blockDim.x vectors
+    void *qwork;       // scratch for QS_GLOBAL
     long long batch;
     int n;
     int budget;        // sweep budget per problem (max_sweeps_per_n * n)
@@ -48,155 +53,167 @@ struct KParams {
 };
 
 // ---------------------------------------------------------------------------
-// Q storage policies.  All rotate the column pair (C, C-1) with
+// Element arithmetic of the eigenvector update.  float rows are processed in
+// packed pairs (one f32x2 instruction updates two rows), double rows singly.
+// Every policy rotates the column pair (C, C-1) as
 //   q_C <- cs q_C + sn q_{C-1},  q_{C-1} <- -sn q_C + cs q_{C-1}
 // which is Q <- Q G for the similarity G^T T G of the chase.
 // ---------------------------------------------------------------------------
+template <typename T>
+struct El;
 
-template <typename T, int NM, int QS>
-struct QStore;
+template <>
+struct El<float> {
+    using E = uint64_t;  // two consecutive rows
+    static constexpr int RPE = 2;
+    struct R {
+        uint64_t c, s, ns;
+    };
+    __device__ static __forceinline__ R make(float cs, float sn) { return {pk2(cs, cs), pk2(sn, sn), pk2(-sn, -sn)}; }
+    __device__ static __forceinline__ void rot(E &x, E &y, const R &r)
+    {
+        const E xo = x;
+        x = fma2(r.c, x, mul2(r.s, y));
+        y = fma2(r.c, y, mul2(r.ns, xo));
+    }
+    __device__ static __forceinline__ E unit(int row, int base)
+    {
+        return pk2(row == base ? 1.0f : 0.0f, row == base + 1 ? 1.0f : 0.0f);
+    }
+    __device__ static __forceinline__ void get(E v, float *out) { upk2(v, out[0], out[1]); }
+};
 
-// Whole Q in registers: q[col][row].
-template <typename T, int NM>
-struct QStore<T, NM, QS_REG> {
-    T q[NM][NM];
+template <>
+struct El<double> {
+    using E = double;
+    static constexpr int RPE = 1;
+    struct R {
+        double c, s, ns;
+    };
+    __device__ static __forceinline__ R make(double cs, double sn) { return {cs, sn, -sn}; }
+    __device__ static __forceinline__ void rot(E &x, E &y, const R &r)
+    {
+        const E xo = x;
+        x = fma(r.c, x, r.s * y);
+        y = fma(r.c, y, r.ns * xo);
+    }
+    __device__ static __forceinline__ E unit(int row, int base) { return row == base ? 1.0 : 0.0; }
+    __device__ static __forceinline__ void get(E v, double *out) { out[0] = v; }
+};
 
-    __device__ __forceinline__ void setup(void *, int) {}
+// Q with rows [0, RR) in registers and rows [RR, RR + MR) in memory (shared
+// or global), streamed one column at a time: the column shared by two
+// successive rotations of a sweep stays in registers (page "perf_steqr":
+// streaming rotation apply).  Memory layout in 16-byte vectors, vector g of
+// column k of thread t at base[(k*G + g)*stride + t]: the lanes of a warp
+// touch consecutive vectors whatever column they are on, so shared memory is
+// accessed without bank conflicts.  Loads are unconditional (every lane's
+// region holds finite values); stores only write columns a lane changed.
+template <typename T, int NM, int RR, int MR>
+struct QMix {
+    using Tr = El<T>;
+    using E = typename Tr::E;
+    static constexpr int RPE = Tr::RPE;
+    static constexpr int NER = RR / RPE;  // register elements per column
+    static constexpr int NEM = MR / RPE;  // memory elements per column
+    static constexpr int G = NEM / 2;     // 16-byte vectors per column
+    static_assert(RR % RPE == 0 && NEM % 2 == 0, "row split must match the vector width");
+    struct V16 {
+        E a, b;
+    };
+
+    E qr[NM][NER > 0 ? NER : 1];
+    E cur[NEM > 0 ? NEM : 1];
+    V16 *base;
+    int stride;
+
+    __device__ __forceinline__ void setup(void *p, int s)
+    {
+        base = reinterpret_cast<V16 *>(p);
+        stride = s;
+    }
+    __device__ __forceinline__ void load(int k, E (&x)[NEM > 0 ? NEM : 1]) const
+    {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const V16 v = base[(k * G + g) * stride];
+            x[2 * g] = v.a;
+            x[2 * g + 1] = v.b;
+        }
+    }
+    __device__ __forceinline__ void store(int k, const E (&x)[NEM > 0 ? NEM : 1]) const
+    {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
+    }
     __device__ __forceinline__ void init_col(int s, int row_of_one)
-    {
-#pragma unroll
-        for (int k = 0; k < NM; ++k) {
-            if (k == s) {
-#pragma unroll
-                for (int r = 0; r < NM; ++r)
-                    q[k][r] = (r == row_of_one) ? T(1) : T(0);
-            }
-        }
-    }
-    __device__ __forceinline__ void begin(int) {}
-    __device__ __forceinline__ void end(int) {}
-    template <int C>
-    __device__ __forceinline__ void rot(T cs, T sn)
-    {
-#pragma unroll
-        for (int r = 0; r < NM; ++r) {
-            T x = q[C][r], y = q[C - 1][r];
-            q[C][r] = fma(cs, x, sn * y);
-            q[C - 1][r] = fma(cs, y, -sn * x);
-        }
-    }
-    // Column s (static s in an unrolled loop) into out[].
-    __device__ __forceinline__ void get_col(int s, T (&out)[NM])
     {
 #pragma unroll
         for (int k = 0; k < NM; ++k)
             if (k == s) {
 #pragma unroll
-                for (int r = 0; r < NM; ++r)
-                    out[r] = q[k][r];
+                for (int j = 0; j < NER; ++j)
+                    qr[k][j] = Tr::unit(row_of_one, j * RPE);
             }
-    }
-};
-
-template <typename T>
-struct Vec16;
-template <>
-struct Vec16<float> {
-    using V = float4;
-    static constexpr int W = 4;
-    __device__ static __forceinline__ void unpack(const V &v, float *x)
-    {
-        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    }
-    __device__ static __forceinline__ V pack(const float *x) { return make_float4(x[0], x[1], x[2], x[3]); }
-};
-template <>
-struct Vec16<double> {
-    using V = double2;
-    static constexpr int W = 2;
-    __device__ static __forceinline__ void unpack(const V &v, double *x)
-    {
-        x[0] = v.x; x[1] = v.y;
-    }
-    __device__ static __forceinline__ V pack(const double *x) { return make_double2(x[0], x[1]); }
-};
-
-// Q in memory (shared or global), streamed one column at a time: the column
-// shared by two successive rotations of a sweep stays in registers (page
-// "perf_steqr": streaming rotation apply).  Layout in 16-byte vectors,
-// element (column k, row group g, thread t) at base[(k*G + g)*stride + t]:
-// the lanes of a warp touch consecutive vectors whatever columns they are
-// on, so shared-memory accesses are free of bank conflicts.
-template <typename T, int NM>
-struct QStream {
-    using VT = Vec16<T>;
-    using V = typename VT::V;
-    static constexpr int W = VT::W;
-    static constexpr int G = (NM + W - 1) / W;
-    static constexpr int NR = G * W;
-    V *base;
-    int stride;
-    T cur[NR];
-
-    __device__ __forceinline__ void setup(void *p, int s)
-    {
-        base = reinterpret_cast<V *>(p);
-        stride = s;
-    }
-    __device__ __forceinline__ void load(int k, T (&x)[NR]) const
-    {
+        if constexpr (NEM > 0) {
+            E x[NEM];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            V v = base[(k * G + g) * stride];
-            VT::unpack(v, &x[g * W]);
+            for (int j = 0; j < NEM; ++j)
+                x[j] = Tr::unit(row_of_one, RR + j * RPE);
+            store(s, x);
         }
     }
-    __device__ __forceinline__ void store(int k, const T (&x)[NR]) const
+    __device__ __forceinline__ void begin(int hi)
     {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-            base[(k * G + g) * stride] = VT::pack(&x[g * W]);
+        if constexpr (NEM > 0)
+            load(hi, cur);
     }
-    __device__ __forceinline__ void init_col(int s, int row_of_one)
+    __device__ __forceinline__ void end(int col, bool st)
     {
-        T x[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-            x[r] = (r == row_of_one) ? T(1) : T(0);
-        store(s, x);
+        if constexpr (NEM > 0)
+            if (st)
+                store(col, cur);
     }
-    __device__ __forceinline__ void begin(int hi) { load(hi, cur); }
-    __device__ __forceinline__ void end(int lo) { store(lo, cur); }
     template <int C>
-    __device__ __forceinline__ void rot(T cs, T sn)
+    __device__ __forceinline__ void rot(T cs, T sn, bool st)
     {
-        T nx[NR];
-        load(C - 1, nx);
+        const typename Tr::R r = Tr::make(cs, sn);
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            T x = cur[r], y = nx[r];
-            cur[r] = fma(cs, x, sn * y);
-            nx[r] = fma(cs, y, -sn * x);
+        for (int j = 0; j < NER; ++j)
+            Tr::rot(qr[C][j], qr[C - 1][j], r);
+        if constexpr (NEM > 0) {
+            E nx[NEM];
+            load(C - 1, nx);
+#pragma unroll
+            for (int j = 0; j < NEM; ++j)
+                Tr::rot(cur[j], nx[j], r);
+            if (st)
+                store(C, cur);
+#pragma unroll
+            for (int j = 0; j < NEM; ++j)
+                cur[j] = nx[j];
         }
-        store(C, cur);
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-            cur[r] = nx[r];
     }
-    __device__ __forceinline__ void get_col(int s, T (&out)[NM])
+    // Column s (static s in an unrolled loop), all stored rows, into out[].
+    __device__ __forceinline__ void get_col(int s, T (&out)[RR + MR])
     {
-        T x[NR];
-        load(s, x);
 #pragma unroll
-        for (int r = 0; r < NM; ++r)
-            out[r] = x[r];
+        for (int k = 0; k < NM; ++k)
+            if (k == s) {
+#pragma unroll
+                for (int j = 0; j < NER; ++j)
+                    Tr::get(qr[k][j], &out[j * RPE]);
+            }
+        if constexpr (NEM > 0) {
+            E x[NEM];
+            load(s, x);
+#pragma unroll
+            for (int j = 0; j < NEM; ++j)
+                Tr::get(x[j], &out[RR + j * RPE]);
+        }
     }
 };
-
-template <typename T, int NM>
-struct QStore<T, NM, QS_SMEM> : QStream<T, NM> {};
-template <typename T, int NM>
-struct QStore<T, NM, QS_GLOBAL> : QStream<T, NM> {};
 
 // Empty store for eigenvalues only.
 template <typename T, int NM>
@@ -204,10 +221,20 @@ struct QNone {
     __device__ __forceinline__ void setup(void *, int) {}
     __device__ __forceinline__ void init_col(int, int) {}
     __device__ __forceinline__ void begin(int) {}
-    __device__ __forceinline__ void end(int) {}
+    __device__ __forceinline__ void end(int, bool) {}
     template <int C>
-    __device__ __forceinline__ void rot(T, T) {}
-    __device__ __forceinline__ void get_col(int, T (&)[NM]) {}
+    __device__ __forceinline__ void rot(T, T, bool) {}
+};
+
+// Row split per storage policy.  Memory rows are padded to whole 16-byte
+// vectors; padding rows stay zero.
+template <typename T, int NM, int QS>
+struct QLayout {
+    static constexpr int W = 16 / (int)sizeof(T);
+    static constexpr int RR = QS == QS_REG ? NM : (QS == QS_HYBRID ? kHybridRegRows : 0);
+    static constexpr int MR = QS == QS_REG ? 0 : ((NM - RR + W - 1) / W) * W;
+    using type = QMix<T, NM, RR, MR>;
+    static constexpr int ROWS = RR + MR;
 };
 
 // ---------------------------------------------------------------------------
@@ -228,12 +255,11 @@ __device__ __forceinline__ void put(T (&a)[NM], int i, T v)
 {
 #pragma unroll
     for (int k = 0; k < NM; ++k)
-        if (i == k)
-            a[k] = v;
+        a[k] = (i == k) ? v : a[k];
 }
 
-// First block [lb, le] containing storage index s, from the boundary mask
-// (bit i set when e_i is an exact zero or i >= n-1).
+// Block [lb, le] containing storage index s, from the boundary mask (bit i
+// set when e_i is an exact zero or i >= n-1).
 __device__ __forceinline__ int block_lo(unsigned zmask, int s)
 {
     unsigned below = s > 0 ? (zmask & ((1u << s) - 1u)) : 0u;
@@ -247,7 +273,7 @@ __device__ __forceinline__ int block_hi(unsigned zmask, int s)
 // ---------------------------------------------------------------------------
 // One problem.
 // ---------------------------------------------------------------------------
-template <typename T, int NM>
+template <typename T, int NM, int KEXIT>
 struct Lane {
     using C_ = Consts<T>;
     T d[NM], e[NM];
@@ -261,8 +287,19 @@ struct Lane {
     T pre, sc, aeff, anorm;
     int jtot, budget;
     int task, m;
-    T f, g;                    // running pair of the chase
-    T lam_lo, lam_hi, cs2, sn2;  // pending 2x2 solve
+    T f, g;        // running pair of the chase
+    T f0, g0;      // seed of the current sweep, (d_m - mu, e_{m-1})
+    T cs2, sn2;    // rotation of a pending 2x2 solve
+    unsigned zeroed;  // off-diagonals set to zero by the deflation test
+    // current pass: positions [lo_l, hi_l] are this lane's (hi_l < 0: none),
+    // and the same as bit masks over C: in range, sweep rotation, 2x2
+    // rotation, first rotation, "e_C <- r", columns this lane changes
+    int hi_l, lo_l;
+    unsigned m_in, m_act, m_22, m_first, m_er, m_touch;
+    // shared-memory mirror of d and e for the settle step's dynamic reads:
+    // entry i of d at mir[i * mstride], of e at mir[(NM + i) * mstride]
+    T *mir;
+    int mstride;
 
     // Storage index s -> caller's index.
     __device__ __forceinline__ int phys(int s) const
@@ -321,7 +358,9 @@ struct Lane {
         revmask = 0;
         iscale = 0;
         pre = sc = aeff = anorm = T(1);
-        f = g = lam_lo = lam_hi = cs2 = sn2 = T(0);
+        f = g = f0 = g0 = cs2 = sn2 = T(0);
+        zeroed = 0;
+        clear_pass();
         if (!live) {
             status = ST_DEAD;
             zmask = ~0u;
@@ -421,22 +460,33 @@ struct Lane {
     }
 
     // Relative deflation test (page "algo_steqr"):
-    // |e_i|^2 <= eps^2 |d_i| |d_{i+1}| + safmin, for i in [lo, le).
+    // |e_i|^2 <= eps^2 |d_i| |d_{i+1}| + safmin, for i in [lo, le).  An
+    // off-diagonal found negligible earlier counts as the exact zero it was
+    // set to (it is never read as a coupling again).
     __device__ __forceinline__ unsigned deflation_mask() const
     {
         unsigned mk = 0;
 #pragma unroll
         for (int i = 0; i < NM - 1; ++i) {
-            if (i >= lo && i < le) {
-                T ae = dabs(e[i]);
-                T tst = ae * ae;
-                T thr = fma(C_::eps2 * dabs(d[i]), dabs(d[i + 1]), C_::safmin);
-                if (tst <= thr)
-                    mk |= 1u << i;
-            }
+            const T ae = dabs(e[i]);
+            const T tst = ae * ae;
+            const T thr = fma(C_::eps2 * dabs(d[i]), dabs(d[i + 1]), C_::safmin);
+            mk |= (tst <= thr) ? (1u << i) : 0u;
         }
-        return mk;
+        const unsigned range = ((1u << le) - 1u) & (~0u << lo);
+        return (mk | zeroed) & range;
     }
+
+    __device__ __forceinline__ void write_mirror() const
+    {
+#pragma unroll
+        for (int i = 0; i < NM; ++i) {
+            mir[i * mstride] = d[i];
+            mir[(NM + i) * mstride] = e[i];
+        }
+    }
+    __device__ __forceinline__ T mir_d(int i) const { return mir[i * mstride]; }
+    __device__ __forceinline__ T mir_e(int i) const { return mir[(NM + i) * mstride]; }
 
     // One settle event.  Returns true while the lane has no chase task and is
     // still running.
@@ -463,21 +513,24 @@ struct Lane {
             dvalid = false;
         }
         if (!dvalid) {
+            write_mirror();
             dmask = deflation_mask();
             dvalid = true;
         }
-        int mm = __ffs((dmask & (~0u << lo)) | (1u << le)) - 1;
+        const int mm = __ffs(dmask | (1u << le)) - 1;
         if (mm < le)
-            put(e, mm, T(0));
+            zeroed |= 1u << mm;  // e_mm <- 0
         if (mm == lo) {  // eigenvalue at lo has converged
             ++lo;
             if (lo > le)
                 close_block();
+            else
+                dmask &= ~0u << lo;
             return true;
         }
-        if (mm == lo + 1) {  // 2x2 direct solve, executed in the next pass
-            T a = pick(d, lo), bb = pick(e, lo), c2 = pick(d, lo + 1);
-            solve2x2(a, bb, c2, lam_lo, lam_hi, cs2, sn2);
+        const T d1 = mir_d(lo), d2 = mir_d(lo + 1), e1 = mir_e(lo);
+        if (mm == lo + 1) {  // 2x2 direct solve, applied in the next pass
+            solve2x2(d1, e1, d2, cs2, sn2);
             task = TASK_2X2;
             m = lo + 1;
             return false;
@@ -487,69 +540,161 @@ struct Lane {
             int cnt = 0;
 #pragma unroll
             for (int i = 0; i < NM - 1; ++i)
-                if (i < n - 1 && e[i] != T(0))
+                if (i < n - 1 && e[i] != T(0) && !((zeroed >> i) & 1u))
                     ++cnt;
             info = cnt;
             status = ST_FAIL;
             return false;
         }
         ++jtot;
-        T d1 = pick(d, lo), d2 = pick(d, lo + 1), e1 = pick(e, lo);
-        T mu = wilkinson_shift(d1, d2, e1);
-        f = pick(d, mm) - mu;
-        g = pick(e, mm - 1);
+        const T mu = wilkinson_shift(d1, d2, e1);
+        f0 = mir_d(mm) - mu;
+        g0 = mir_e(mm - 1);
         m = mm;
         task = TASK_SWEEP;
         return false;
     }
 
-    __device__ __forceinline__ int task_hi() const { return m; }
-    __device__ __forceinline__ int task_lo() const { return lo + 1; }
+    __device__ __forceinline__ bool has_task() const { return status == ST_RUN && task != TASK_NONE; }
 
-    // Rotation on the pair (C, C-1) of the current task, if C is in its range.
-    template <int C, class QS>
-    __device__ __forceinline__ void chase_at(QS &Q)
+    __device__ __forceinline__ void clear_pass()
     {
-        if (task == TASK_SWEEP && C <= m && C > lo) {
-            T cs, sn, r;
-            lartg(f, g, cs, sn, r);
-            T a = d[C], b = e[C - 1], cc = d[C - 1];
-            // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP)
-            T p1 = fma(cs, a, sn * b);
-            T p2 = fma(cs, b, sn * cc);
-            T dn = fma(cs, p1, sn * p2);
-            T en = fma(cs, p2, -sn * p1);
-            d[C] = dn;
-            d[C - 1] = (a + cc) - dn;
-            e[C - 1] = en;
-            if (C < m)
-                e[C] = r;
-            if constexpr (C >= 2) {
-                if (C - 1 > lo) {
-                    T eo = e[C - 2];
-                    g = sn * eo;  // new bulge
-                    e[C - 2] = cs * eo;
-                    f = en;
-                }
-            }
-            Q.template rot<C>(cs, sn);
-        } else if (task == TASK_2X2 && C == lo + 1) {
-            d[C - 1] = lam_lo;
-            d[C] = lam_hi;
-            e[C - 1] = T(0);
-            Q.template rot<C>(cs2, sn2);
+        hi_l = -1;
+        lo_l = NM;
+        m_in = m_act = m_22 = m_first = m_er = m_touch = 0u;
+    }
+
+    __device__ __forceinline__ void prepare_pass()
+    {
+        if (!has_task()) {
+            clear_pass();
+            return;
         }
+        hi_l = m;
+        lo_l = lo + 1;
+        const unsigned upto = hi_l >= 31 ? ~0u : ((2u << hi_l) - 1u);  // bits 0..hi_l
+        m_in = upto & (~0u << lo_l);
+        m_touch = upto & (~0u << lo);
+        if (task == TASK_2X2) {
+            m_act = 0u;
+            m_22 = m_in;
+            m_first = 0u;
+        } else {
+            m_act = m_in;
+            m_22 = 0u;
+            m_first = 1u << hi_l;
+        }
+        m_er = m_act & ~(1u << hi_l);
+    }
+
+    // Position C of a pass: rotation on the pair (C, C-1) for lanes whose
+    // task covers C, identity (lartg of (1, 0)) for the others.
+    template <int C, class QT>
+    __device__ __forceinline__ void chase_at(QT &Q)
+    {
+        const bool in = (m_in >> C) & 1u;
+        const bool act = (m_act >> C) & 1u;
+        const bool a22 = (m_22 >> C) & 1u;
+        const bool first = (m_first >> C) & 1u;
+        const T fa = first ? f0 : f;
+        const T ga = first ? g0 : g;
+        T cs, sn, r;
+        lartg(act ? fa : T(1), act ? ga : T(0), cs, sn, r);
+        cs = a22 ? cs2 : cs;
+        sn = a22 ? sn2 : sn;
+        const T a = d[C], b = e[C - 1], cc = d[C - 1];
+        // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP)
+        const T p1 = fma(cs, a, sn * b);
+        const T p2 = fma(cs, b, sn * cc);
+        const T dn = fma(cs, p1, sn * p2);
+        const T en = fma(cs, p2, -sn * p1);
+        if constexpr (sizeof(T) == 4) {
+            // float: every entry from its explicit formula, which the
+            // identity rotation reproduces exactly (up to the sign of a zero)
+            const T q1 = fma(cs, cc, -sn * b);
+            const T q2 = fma(cs, b, -sn * a);
+            d[C] = dn;
+            d[C - 1] = fma(cs, q1, -sn * q2);
+        } else {
+            // double: trace identity for d_{C-1} and a select (the integer
+            // pipe is idle next to FP64)
+            d[C] = in ? dn : a;
+            d[C - 1] = in ? (a + cc) - dn : cc;
+        }
+        e[C - 1] = a22 ? T(0) : en;
+        e[C] = ((m_er >> C) & 1u) ? r : e[C];
+        if constexpr (C >= 2) {
+            const T eo = e[C - 2];
+            g = sn * eo;  // new bulge
+            e[C - 2] = cs * eo;
+        }
+        f = en;
+        Q.template rot<C>(cs, sn, (m_touch >> C) & 1u);
+    }
+
+    // One pass over positions rhi .. (group boundary <= rlo).
+    template <class QT>
+    __device__ __forceinline__ void run_pass(QT &Q, int rhi, int rlo)
+    {
+        Q.begin(rhi);
+        int last = 0;
+        switch (rhi) {
+#define BSTQ_POS(C)                                                          \
+    case C:                                                                  \
+        if constexpr (C <= NM - 1) {                                         \
+            chase_at<C>(Q);                                                  \
+            if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                 \
+                if (C - 1 < rlo) {                                           \
+                    last = C - 1;                                            \
+                    goto pass_done;                                          \
+                }                                                            \
+            }                                                                \
+        }                                                                    \
+        [[fallthrough]];
+            BSTQ_POS(31) BSTQ_POS(30) BSTQ_POS(29) BSTQ_POS(28) BSTQ_POS(27) BSTQ_POS(26)
+            BSTQ_POS(25) BSTQ_POS(24) BSTQ_POS(23) BSTQ_POS(22) BSTQ_POS(21) BSTQ_POS(20)
+            BSTQ_POS(19) BSTQ_POS(18) BSTQ_POS(17) BSTQ_POS(16) BSTQ_POS(15) BSTQ_POS(14)
+            BSTQ_POS(13) BSTQ_POS(12) BSTQ_POS(11) BSTQ_POS(10) BSTQ_POS(9) BSTQ_POS(8)
+            BSTQ_POS(7) BSTQ_POS(6) BSTQ_POS(5) BSTQ_POS(4) BSTQ_POS(3) BSTQ_POS(2)
+            BSTQ_POS(1)
+#undef BSTQ_POS
+        default:
+            break;
+        }
+        last = 0;
+    pass_done:
+        Q.end(last, (m_touch >> last) & 1u);
+    }
+
+    // Nested form of a pass: the lane runs exactly its own positions.
+    template <int C, class QT>
+    __device__ __forceinline__ void own_positions(QT &Q)
+    {
+        if constexpr (C >= 1) {
+            if (C <= hi_l && C >= lo_l)
+                chase_at<C>(Q);
+            own_positions<C - 1>(Q);
+        }
+    }
+    template <class QT>
+    __device__ __forceinline__ void run_pass_nested(QT &Q)
+    {
+        Q.begin(hi_l);
+        own_positions<NM - 1>(Q);
+        Q.end(lo_l - 1, true);
     }
 
     __device__ __forceinline__ void post_pass()
     {
         if (task == TASK_2X2) {
+            zeroed |= 1u << lo;  // e_lo of the solved 2x2 block
             lo += 2;
             if (lo > le)
                 close_block();
         }
         task = TASK_NONE;
         dvalid = false;
+        clear_pass();
     }
 };
 
@@ -558,62 +703,47 @@ struct Lane {
 // ---------------------------------------------------------------------------
 template <typename T, int NM, bool WANTZ, int QS>
 struct QFor {
-    using type = QStore<T, NM, QS>;
+    using type = typename QLayout<T, NM, QS>::type;
+    static constexpr int ROWS = QLayout<T, NM, QS>::ROWS;
 };
 template <typename T, int NM, int QS>
 struct QFor<T, NM, false, QS> {
     using type = QNone<T, NM>;
+    static constexpr int ROWS = 1;
 };
-
-// Compile-time loop over the chase positions C = top, top-1, ..., 1; the
-// warp (or, nested, the lane) skips positions outside [rlo, rhi].
-template <int C>
-struct ChaseLoop {
-    template <class LaneT, class QT>
-    __device__ static __forceinline__ void run(LaneT &L, QT &Q, int rhi, int rlo)
-    {
-        if (!(C > rhi || C < rlo))
-            L.template chase_at<C>(Q);
-        ChaseLoop<C - 1>::run(L, Q, rhi, rlo);
-    }
-};
-template <>
-struct ChaseLoop<0> {
-    template <class LaneT, class QT>
-    __device__ static __forceinline__ void run(LaneT &, QT &, int, int) {}
-};
-
-template <int NM, class LaneT, class QT>
-__device__ __forceinline__ void chase_pass(LaneT &L, QT &Q, int rhi, int rlo)
-{
-    ChaseLoop<NM - 1>::run(L, Q, rhi, rlo);
-}
 
 template <typename T, int NM, bool WANTZ, int QS, int SCHED>
 __global__ void lane_kernel(KParams p)
 {
     extern __shared__ uint4 smem_raw[];
     using QT = typename QFor<T, NM, WANTZ, QS>::type;
+    constexpr int KEXIT = WANTZ ? 4 : 2;
     const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool live = b < p.batch;
 
-    Lane<T, NM> L;
+    // dynamic shared memory: [memory rows of Q (shared / hybrid)] [mirror]
+    constexpr bool kQShared = WANTZ && (QS == QS_SMEM || QS == QS_HYBRID);
+    constexpr size_t kQBytesPerLane = kQShared ? size_t(NM) * QLayout<T, NM, QS>::MR * sizeof(T) : 0;
+    Lane<T, NM, KEXIT> L;
+    L.mir = reinterpret_cast<T *>(reinterpret_cast<char *>(smem_raw) + kQBytesPerLane * blockDim.x) +
+            threadIdx.x;
+    L.mstride = blockDim.x;
     L.load(p, b, live);
     QT Q;
-    if (WANTZ) {
-        if (QS == QS_SMEM) {
+    if constexpr (WANTZ) {
+        if constexpr (kQShared) {
             Q.setup(reinterpret_cast<char *>(smem_raw) + 16 * threadIdx.x, blockDim.x);
-        } else if (QS == QS_GLOBAL) {
-            constexpr int G = (NM * (int)sizeof(T) + 15) / 16;
+        } else if constexpr (QS == QS_GLOBAL) {
+            constexpr int G = QLayout<T, NM, QS>::MR * (int)sizeof(T) / 16;
             char *base = reinterpret_cast<char *>(p.qwork) +
                          16ll * ((long long)blockIdx.x * NM * G * blockDim.x + threadIdx.x);
             Q.setup(base, blockDim.x);
         }
-        if (L.status == ST_RUN) {
+        // every lane initialises its Q (dead and poisoned lanes too: the
+        // memory rows are read unconditionally during the passes)
 #pragma unroll
-            for (int s = 0; s < NM; ++s)
-                Q.init_col(s, s < L.n ? L.phys(s) : s);
-        }
+        for (int s = 0; s < NM; ++s)
+            Q.init_col(s, (L.status == ST_RUN && s < L.n) ? L.phys(s) : s);
     }
 
     if (SCHED == SCHED_FLAT) {
@@ -623,18 +753,15 @@ __global__ void lane_kernel(KParams p)
                 if (need)
                     need = L.settle_step();
             }
-            const bool has = (L.status == ST_RUN) && (L.task != TASK_NONE);
+            const bool has = L.has_task();
             if (!__any_sync(FULL, has))
                 break;
-            const int rhi = __reduce_max_sync(FULL, has ? L.task_hi() : -1);
-            const int rlo = __reduce_min_sync(FULL, has ? L.task_lo() : NM);
+            L.prepare_pass();
+            const int rhi = __reduce_max_sync(FULL, L.hi_l);
+            const int rlo = __reduce_min_sync(FULL, L.lo_l);
+            L.run_pass(Q, rhi, rlo);
             if (has)
-                Q.begin(L.task_hi());
-            chase_pass<NM>(L, Q, rhi, rlo);
-            if (has) {
-                Q.end(L.task_lo() - 1);
                 L.post_pass();
-            }
         }
     } else {
         while (L.status == ST_RUN) {
@@ -642,10 +769,8 @@ __global__ void lane_kernel(KParams p)
                 L.settle_step();
                 continue;
             }
-            const int rhi = L.task_hi(), rlo = L.task_lo();
-            Q.begin(rhi);
-            chase_pass<NM>(L, Q, rhi, rlo);
-            Q.end(rlo - 1);
+            L.prepare_pass();
+            L.run_pass_nested(Q);
             L.post_pass();
         }
     }
@@ -692,11 +817,11 @@ __global__ void lane_kernel(KParams p)
     for (int s = 0; s < NM; ++s)
         if (s < n)
             dout[pos[s]] = L.d[s];
-    if (WANTZ) {
+    if constexpr (WANTZ) {
 #pragma unroll
         for (int s = 0; s < NM; ++s) {
             if (s < n) {
-                T col[NM];
+                T col[QFor<T, NM, WANTZ, QS>::ROWS];
                 Q.get_col(s, col);
                 T *qc = qout + (long long)pos[s] * n;
 #pragma unroll

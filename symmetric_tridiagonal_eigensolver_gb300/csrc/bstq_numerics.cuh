@@ -1,10 +1,17 @@
-// Device building blocks of the steqr iteration: machine constants, the
-// reciprocal square root, lartg, the copysign shift and the 2x2 direct solve.
+// Device building blocks of the steqr iteration: machine constants, Newton-
+// Raphson reciprocal / square-root kernels, lartg, the copysign shift and the
+// 2x2 direct solve.
 //
 // Sources: BatchLAS page "algo_steqr" (deflation criterion, scaling, shift,
 // Givens rotation, EXP update, 2x2 solve) and BatchLAS page "perf_steqr",
-// section "CTA STEQR: chase micro-structure decisions" (rsqrt + one Newton
-// step, range guard, g = 0 select).
+// section "CTA STEQR: chase micro-structure decisions" (hardware reciprocal
+// square root plus one Newton step; the g = 0 case returns (1, 0, f) through
+// a final select so identity rotations do not diverge).
+//
+// The division, reciprocal and square-root helpers here are our own
+// Newton-Raphson refinements of the hardware approximations (rcp.approx,
+// rsqrt.approx); the solver only needs them to be accurate to about an ulp
+// and deterministic, not correctly rounded.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -14,8 +21,7 @@ namespace bstq {
 
 // Machine constants (LAPACK convention; the pages name but do not define
 // them): eps = unit roundoff, safmin = smallest normal, ssfmax =
-// sqrt(1/safmin)/3, ssfmin = sqrt(safmin)/eps^2.  The lartg fast path is
-// valid while max(|f|,|g|) lies in (sqrt(safmin), sqrt(safmax/2)).
+// sqrt(1/safmin)/3, ssfmin = sqrt(safmin)/eps^2.
 template <typename T>
 struct Consts;
 
@@ -27,8 +33,6 @@ struct Consts<float> {
     static constexpr float ssfmax = 0x1p63f / 3.0f;
     static constexpr float ssfmin = 0x1p-15f;
     static constexpr float prescale = 0x1p24f;
-    static constexpr float rt_lo = 0x1p-63f;
-    static constexpr float rt_hi = 6.5219089e18f;  // just below 2^62.5
 };
 
 template <>
@@ -39,16 +43,16 @@ struct Consts<double> {
     static constexpr double ssfmax = 0x1p511 / 3.0;
     static constexpr double ssfmin = 0x1p-405;
     static constexpr double prescale = 0x1p53;
-    static constexpr double rt_lo = 0x1p-511;
-    static constexpr double rt_hi = 4.7403759540545887e153;  // just below 2^510.5
 };
 
 __device__ __forceinline__ float dabs(float x) { return fabsf(x); }
 __device__ __forceinline__ double dabs(double x) { return fabs(x); }
 
-// 1/sqrt(x) for a normal, finite x > 0.
-// float: hardware approximation (rel. error < 2^-22) plus one Newton-Raphson
-// step y <- y + y (1 - x y^2) / 2, as perf_steqr describes.
+// ---------------------------------------------------------------------------
+// Reciprocal square root of a normal, finite x > 0.
+// float: hardware approximation (relative error below 2^-22) and one
+// Newton-Raphson step y <- y + y (1 - x y^2) / 2.
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ float rsqrt_nr(float x)
 {
     float y;
@@ -73,42 +77,121 @@ __device__ __forceinline__ double rsqrt_nr(double x)
     return fma(y, v, y);
 }
 
-// sqrt(1 + x^2) without overflow for large |x|.
+// Reciprocal of a normal x: hardware approximation, then Newton-Raphson
+// y <- y (2 - x y) (float) or the third-order step y <- y (1 + e + e^2),
+// e = 1 - x y (double).
+__device__ __forceinline__ float rcp_nr(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    float e = fmaf(-x, y, 1.0f);
+    return fmaf(y, e, y);
+}
+__device__ __forceinline__ double rcp_nr(double x)
+{
+    double y;
+    asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(y) : "d"(x));
+    double e = fma(-x, y, 1.0);
+    double e2 = fma(e, e, e);
+    return fma(y, e2, y);
+}
+
+// a / b: quotient from the reciprocal plus one residual correction
+// q + (a - b q) / b.
+template <typename T>
+__device__ __forceinline__ T div_nr(T a, T b)
+{
+    T y = rcp_nr(b);
+    T q = a * y;
+    T r = fma(-b, q, a);
+    return fma(r, y, q);
+}
+
+// sqrt(x) for x >= 1 (the only use): s = x rsqrt(x) with one correction
+// s + (x - s^2) / (2 s).
+template <typename T>
+__device__ __forceinline__ T sqrt_nr(T x)
+{
+    T y = rsqrt_nr(x);
+    T s = x * y;
+    T r = fma(-s, s, x);
+    return fma(T(0.5) * y, r, s);
+}
+
+// sqrt(1 + x^2) without overflow, branch free: with w = max(1, |x|) and
+// v = min(1, |x|), it equals w sqrt(1 + (v/w)^2).
 template <typename T>
 __device__ __forceinline__ T hyp1(T x)
 {
     T ax = dabs(x);
-    if (ax <= T(1))
-        return sqrt(T(1) + ax * ax);
-    T y = T(1) / ax;
-    return ax * sqrt(T(1) + y * y);
+    T w = fmax(T(1), ax);
+    T v = fmin(T(1), ax);
+    T q = div_nr(v, w);
+    return w * sqrt_nr(fma(q, q, T(1)));
 }
 
-// lartg: G(c,s) = [[c,-s],[s,c]] with G^T [f; g] = [r; 0].
-// g == 0 gives (1, 0, f) through a final select (no early return).
-// In-range inputs use r2 = f^2 + g^2, y = rsqrt(r2): c = f y, s = g y,
-// r = r2 y.  Anything else (including NaN) takes the max-scaled formula.
-template <typename T>
-__device__ __forceinline__ void lartg(T f, T g, T &c, T &s, T &r)
+// ---------------------------------------------------------------------------
+// lartg: G(c,s) = [[c,-s],[s,c]] with G^T [f; g] = [r; 0], r = hypot(f, g);
+// g == 0 returns (1, 0, f) through a final select.
+//
+// float: r2 = f^2 + g^2 and y = rsqrt(r2) give c = f y, s = g y, r = r2 y
+// while r2 is a comfortably normal number; otherwise (a rare, divergent
+// branch) f and g are first multiplied by the power of two 2^-k that brings
+// max(|f|, |g|) into [1, 2), so the sum of squares can neither overflow nor
+// underflow, and r is scaled back by 2^k (page "perf_steqr": in-range fast
+// path, scaled path for the rest).
+// double: always the scaled form; the exponent arithmetic runs on the
+// integer pipe, which is idle next to the FP64 pipe.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void lartg_scaled(float f, float g, float &c, float &s, float &r)
 {
-    T w = fmax(dabs(f), dabs(g));
-    T r2 = fma(f, f, g * g);
-    T y = rsqrt_nr(r2);
+    const unsigned fb = __float_as_uint(f) & 0x7fffffffu;
+    const unsigned gb = __float_as_uint(g) & 0x7fffffffu;
+    int ew = (int)(max(fb, gb) >> 23);
+    ew = min(max(ew, 1), 253);
+    const float sc = __uint_as_float((unsigned)(254 - ew) << 23);  // 2^(127-ew)
+    const float isc = __uint_as_float((unsigned)ew << 23);         // 2^(ew-127)
+    const float fs = f * sc, gs = g * sc;
+    const float r2 = fmaf(fs, fs, gs * gs);
+    const float y = rsqrt_nr(r2);
+    c = fs * y;
+    s = gs * y;
+    r = (r2 * y) * isc;
+}
+
+__device__ __forceinline__ void lartg(float f, float g, float &c, float &s, float &r)
+{
+    const float r2 = fmaf(f, f, g * g);
+    const float y = rsqrt_nr(r2);
     c = f * y;
     s = g * y;
     r = r2 * y;
-    if (!(w > Consts<T>::rt_lo && w < Consts<T>::rt_hi)) {
-        T z = fmin(dabs(f), dabs(g)) / w;
-        T h = w * sqrt(T(1) + z * z);
-        c = f / h;
-        s = g / h;
-        r = h;
-    }
-    if (g == T(0)) {
-        c = T(1);
-        s = T(0);
-        r = f;
-    }
+    if (!(r2 >= 0x1p-100f && r2 <= 0x1p100f))
+        lartg_scaled(f, g, c, s, r);
+    const bool z = g == 0.0f;
+    c = z ? 1.0f : c;
+    s = z ? 0.0f : s;
+    r = z ? f : r;
+}
+
+__device__ __forceinline__ void lartg(double f, double g, double &c, double &s, double &r)
+{
+    const unsigned fh = (unsigned)__double2hiint(f) & 0x7fffffffu;
+    const unsigned gh = (unsigned)__double2hiint(g) & 0x7fffffffu;
+    int ew = (int)(max(fh, gh) >> 20);
+    ew = min(max(ew, 1), 2045);
+    const double sc = __hiloint2double((2046 - ew) << 20, 0);  // 2^(1023-ew)
+    const double isc = __hiloint2double(ew << 20, 0);          // 2^(ew-1023)
+    const double fs = f * sc, gs = g * sc;
+    const double r2 = fma(fs, fs, gs * gs);
+    const double y = rsqrt_nr(r2);
+    c = fs * y;
+    s = gs * y;
+    r = (r2 * y) * isc;
+    const bool z = (gh | (unsigned)__double2loint(g)) == 0u;
+    c = z ? 1.0 : c;
+    s = z ? 0.0 : s;
+    r = z ? f : r;
 }
 
 // Copysign shift from the 2x2 block (d1, e1; e1, d2) at the converging end:
@@ -116,28 +199,52 @@ __device__ __forceinline__ void lartg(T f, T g, T &c, T &s, T &r)
 template <typename T>
 __device__ __forceinline__ T wilkinson_shift(T d1, T d2, T e1)
 {
-    T g = (d2 - d1) / (T(2) * e1);
+    T g = div_nr(d2 - d1, T(2) * e1);
     T r = hyp1(g);
-    return d1 - e1 / (g + copysign(r, g));
+    return d1 - div_nr(e1, g + copysign(r, g));
 }
 
 // Direct solve of the 2x2 block [[a, b], [b, c2]] (b != 0): the rotation
 // with tangent t, the smaller root of t^2 + 2 tau t - 1 = 0,
-// tau = (c2 - a) / (2 b), diagonalises it; the eigenvalues are a - t b and
-// c2 + t b.  Returns them with (cs, sn) of that rotation written in the
-// chase's column convention for the pair (k + 1, k):
+// tau = (c2 - a) / (2 b), diagonalises it (eigenvalues a - t b and
+// c2 + t b).  Returns (cs, sn) of that rotation in the chase's column
+// convention for the pair (k + 1, k) with k the block's first index:
 //   q_{k+1} <- cs q_{k+1} + sn q_k,  q_k <- -sn q_{k+1} + cs q_k.
 template <typename T>
-__device__ __forceinline__ void solve2x2(T a, T b, T c2, T &lam_lo, T &lam_hi, T &cs, T &sn)
+__device__ __forceinline__ void solve2x2(T a, T b, T c2, T &cs, T &sn)
 {
-    T tau = (c2 - a) / (T(2) * b);
+    T tau = div_nr(c2 - a, T(2) * b);
     T sgn = tau < T(0) ? T(-1) : T(1);
-    T t = sgn / (dabs(tau) + hyp1(tau));
-    T cq = T(1) / hyp1(t);
-    lam_lo = a - t * b;
-    lam_hi = c2 + t * b;
+    T t = div_nr(sgn, dabs(tau) + hyp1(tau));
+    T cq = rcp_nr(hyp1(t));
     cs = cq;
     sn = t * cq;
+}
+
+// ---------------------------------------------------------------------------
+// Packed float pairs (f32x2): two FP32 lanes per instruction.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk2(float a, float b)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 }  // namespace bstq

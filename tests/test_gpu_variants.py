@@ -27,7 +27,7 @@ def test_flat_equals_nested(dt, n, jobz):
     check_parity(d, e, *a, oracle_ref(d, e, jobz=jobz), what=f"flat {n}")
 
 
-@pytest.mark.parametrize("dt,n,qs", [(np.float32, 16, 3), (np.float32, 24, 3), (np.float64, 12, 2),
+@pytest.mark.parametrize("dt,n,qs", [(np.float32, 16, 3), (np.float32, 16, 2), (np.float32, 32, 3), (np.float64, 12, 2),
                                      (np.float64, 12, 3), (np.float64, 16, 3)])
 def test_qstore_variants_agree(dt, n, qs):
     d, e = inputs.normal_problems(n, 5000, dt, seed=7)
