@@ -133,6 +133,40 @@ int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
                     void *h_d, const void *h_e, void *h_Q, int32_t *h_info,
                     void *dev, void *stream, const bstq_params *p);
 
+/*
+ * Allocation-free variant of bstq_solve_ex for jobz == BSTQ_JOBZ_V (the
+ * BatchLAS pages have no counterpart; this is a library convenience).
+ *
+ * For callers that cannot allocate device memory when they solve: code that
+ * runs while a CUDA graph is being captured, inside an allocator callback, in
+ * a plugin handed fixed buffers by its host framework, or in a real-time loop
+ * that must never call cudaMalloc.  Instead of a caller-sized `work` buffer,
+ * the eigenvector scratch lives in a 64 MiB array compiled into the library;
+ * every GPU that loads the library reserves it until the process exits.
+ * The call itself allocates nothing and calls no allocating routine.
+ *   d, e, Q   as for bstq_solve (device memory); Q is required.
+ *   info      device int32[batch], receives the per-problem status.
+ *   p         optional parameters; p->qstore is ignored.
+ * Sizes: n in 13..32 for float and 9..32 for double (smaller problems keep Q
+ * in registers and need no scratch at all: call bstq_solve with a `work`
+ * buffer of align256(4 * batch) bytes, which only receives info; for them
+ * this call returns -10).
+ * Returns 0; -2 when jobz is not BSTQ_JOBZ_V; -4 when the problems need more
+ * scratch than the array holds (n_pad^2 * sizeof(element) bytes per problem
+ * slot, n_pad = n rounded up to 12, 16, 24 or 32, slots = batch rounded up to
+ * the block size; e.g. about 58,000 double problems of n <= 12 fit, or 16,000
+ * float problems of n <= 32); other codes as bstq_solve_ex.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and the kernel overwrites the part it uses
+ * before reading it, so nothing needs clearing between calls; calls that can
+ * overlap on the GPU (different streams, or graphs replayed concurrently)
+ * race on the array and must be serialised by the caller.
+ */
+int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                       void *d, const void *e, void *Q, int32_t *info,
+                       void *stream, const bstq_params *p);
+
 /* Description of the kernel the library would launch (for tests and
  * benchmarks): fills up to `len` bytes of `buf` with a NUL-terminated string
  * such as "lane<f32,16,V,shared,flat> tpb=224 grid=147" and returns 0, or

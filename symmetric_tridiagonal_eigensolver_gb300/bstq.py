@@ -25,7 +25,7 @@ MAX_N = 32
 # Every symbol include/bstq.h declares.
 EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",
            "bstq_host_work_size", "bstq_solve_host", "bstq_describe",
-           "bstq_status_string", "bstq_version", "bstq_last_error")
+           "bstq_status_string", "bstq_version", "bstq_last_error", "bstq_solve_noalloc")
 
 
 class Params(ctypes.Structure):
@@ -82,6 +82,9 @@ def load(path: str = LIB_PATH):
         lib.bstq_version.argtypes = []
         lib.bstq_last_error.restype = ctypes.c_char_p
         lib.bstq_last_error.argtypes = []
+        lib.bstq_solve_noalloc.restype = ctypes.c_int
+        lib.bstq_solve_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp,
+                                           vp, P]
         _lib = lib
         return lib
 
@@ -189,3 +192,18 @@ def solve_host(h_d, h_e, h_Q, h_info, dev, stream=None, jobz: bool = True, **par
                                 _stream_handle(stream), ctypes.byref(p))
     if rc != 0:
         raise BstqError(rc, "bstq_solve_host")
+
+
+def solve_noalloc(d, e, Q, info, stream=None, **params):
+    """bstq_solve_noalloc on CUDA tensors (jobz = V): d (batch, n) in/out,
+    e (batch, n-1), Q (batch, n, n) and info (batch,) int32 caller-owned; the
+    eigenvector scratch is the library's fixed device array.  Returns
+    (d, Q viewed with Q[b, :, j] the j-th eigenvector, info)."""
+    batch, n = d.shape
+    p = _params(**params)
+    e_ptr = e.data_ptr() if e is not None and e.numel() else None
+    rc = load().bstq_solve_noalloc(_dtype_code(d.dtype), JOBZ_V, int(n), int(batch), d.data_ptr(), e_ptr,
+                                   Q.data_ptr(), info.data_ptr(), _stream_handle(stream), ctypes.byref(p))
+    if rc != 0:
+        raise BstqError(rc, "bstq_solve_noalloc")
+    return d, Q.transpose(1, 2), info

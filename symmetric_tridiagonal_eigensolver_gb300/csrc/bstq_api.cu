@@ -415,3 +415,104 @@ extern "C" const char *bstq_status_string(int code)
 extern "C" const char *bstq_version(void) { return "bstq 0.1.0 sm_103a"; }
 
 extern "C" const char *bstq_last_error(void) { return g_last_error; }
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory at the moment they solve: code
+// running inside a captured CUDA graph or a custom allocator's hook, plugins
+// that are handed fixed buffers by a host framework, or real-time loops that
+// must never call cudaMalloc.  bstq_solve needs a `work` buffer whose size
+// depends on the launch; this variant instead keeps the eigenvector scratch
+// of the global-memory Q kernel in a fixed array that lives in the library's
+// own device image.  The array is reserved on every GPU that loads this
+// library and stays reserved until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol's name only stands for the array; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+int noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return bstq::cuda_fail(err, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return BSTQ_ERR_NODEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess)
+            return bstq::cuda_fail(err, "cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return 0;
+}
+
+}  // namespace
+
+extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, void *d,
+                                  const void *e, void *Q, int32_t *info, void *stream,
+                                  const bstq_params *p)
+{
+    int rc = check_args(dtype, jobz, n, batch, p);
+    if (rc)
+        return rc;
+    if (jobz != BSTQ_JOBZ_V)
+        return -2;
+    if (batch == 0)
+        return 0;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    if (!d || misaligned(d, elem))
+        return -5;
+    if ((n > 1 && !e) || misaligned(e, elem))
+        return -6;
+    if (!Q || misaligned(Q, elem))
+        return -7;
+    if (!info || misaligned(info, 4))
+        return -8;
+    bstq_params q = p ? *p : bstq_params{};
+    q.qstore = BSTQ_QSTORE_GLOBAL;
+    Plan pl;
+    rc = make_plan(dtype, jobz, n, batch, &q, pl);
+    if (rc)
+        return rc;
+    if (pl.k->qs != QS_GLOBAL)
+        return -10;
+    if (pl.qwork_bytes > kNoAllocScratchBytes)
+        return -4;  // more problems than the fixed scratch holds
+    void *scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc)
+        return rc;
+    KParams kp;
+    kp.d = d;
+    kp.e = e;
+    kp.Q = Q;
+    kp.info = info;
+    kp.qwork = scratch;
+    kp.batch = batch;
+    kp.n = n;
+    kp.budget = (q.max_sweeps_per_n ? q.max_sweeps_per_n : 30) * n;
+    kp.sort = q.no_sort ? 0 : 1;
+    if (pl.smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "cudaFuncSetAttribute");
+    }
+    void *args[] = {&kp};
+    cudaError_t err = cudaLaunchKernel(pl.k->fn, dim3((unsigned)pl.grid), dim3(pl.tpb), args, pl.smem,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? 0 : cuda_fail(err, "cudaLaunchKernel");
+}

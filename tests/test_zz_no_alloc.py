@@ -1,0 +1,67 @@
+"""bstq_solve_noalloc: the allocation-free entry point for callers that must
+not allocate device memory while they solve (graph capture, allocator hooks,
+fixed-buffer plugins, real-time loops).  It keeps the eigenvector scratch in a
+fixed array inside the library.  These tests call it through the C ABI, twice
+in a row (the array keeps the previous call's contents), and compare with the
+regular entry point under the parity tolerances.  This file is collected
+last so that a run stopping at the first failure has run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from symmetric_tridiagonal_eigensolver_gb300 import inputs
+from tests import helpers as H
+from tests.gpu_helpers import orth_err, run_gpu, tri_residual
+
+pytestmark = pytest.mark.gpu
+
+CASES = [(np.float64, 12, 3000), (np.float32, 16, 2000), (np.float64, 32, 700), (np.float32, 29, 1100)]
+
+
+def _noalloc(d, e):
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    lib = bstq.load()
+    dev = torch.device("cuda:0")
+    batch, n = d.shape
+    dg = torch.from_numpy(np.ascontiguousarray(d)).to(dev)
+    eg = torch.from_numpy(np.ascontiguousarray(e)).to(dev)
+    Q = torch.full((batch, n, n), float("nan"), dtype=dg.dtype, device=dev)
+    info = torch.full((batch,), 7, dtype=torch.int32, device=dev)
+    code = bstq.F32 if d.dtype == np.float32 else bstq.F64
+    stream = torch.cuda.current_stream()
+    rc = lib.bstq_solve_noalloc(code, bstq.JOBZ_V, n, batch, dg.data_ptr(), eg.data_ptr(),
+                                Q.data_ptr(), info.data_ptr(), ctypes.c_void_p(stream.cuda_stream), None)
+    assert rc == 0, bstq.status_string(rc)
+    torch.cuda.synchronize()
+    return dg.cpu().numpy(), Q.transpose(1, 2).cpu().numpy(), info.cpu().numpy()
+
+
+@pytest.mark.parametrize("dt,n,batch", CASES)
+def test_noalloc_matches_regular_entry_point_twice(dt, n, batch):
+    for call in range(2):
+        d, e = inputs.normal_problems(n, batch, dt, seed=40 + call)
+        lam, Q, info = _noalloc(d, e)
+        lam_r, Q_r, info_r = run_gpu(d, e)
+        assert np.array_equal(info, info_r) and np.all(info == 0)
+        tn = H.norm1(d, e).astype(np.float64)
+        eps = H.eps_of(dt)
+        assert np.all(np.abs(lam.astype(np.float64) - lam_r).max(1) <= H.lam_tol(n, dt, tn))
+        assert not np.any(np.isnan(Q))
+        assert np.all(tri_residual(d, e, lam, Q) <= 64 * n * eps * tn)
+        assert np.all(orth_err(Q) <= 64 * n * eps)
+
+
+def test_noalloc_rejects_what_it_cannot_hold():
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    lib = bstq.load()
+    dummy = torch.empty(64, dtype=torch.float64, device="cuda")
+    p = dummy.data_ptr()
+    # more float64 n = 32 problems than 64 MiB of scratch holds: refused, no launch
+    assert lib.bstq_solve_noalloc(bstq.F64, bstq.JOBZ_V, 32, 1 << 20, p, p, p, p, None, None) == -4
+    # eigenvalues only need no scratch: this entry point is for jobz = V
+    assert lib.bstq_solve_noalloc(bstq.F64, bstq.JOBZ_N, 32, 10, p, p, p, p, None, None) == -2
+    # small n keeps Q in registers (no scratch kernel for it)
+    assert lib.bstq_solve_noalloc(bstq.F32, bstq.JOBZ_V, 8, 10, p, p, p, p, None, None) == -10
