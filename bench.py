@@ -44,8 +44,32 @@ COMPANIONS = [dict(dtype="float32", n=8, batch=65536, jobz=True),
 # Context only: steqr_cta float n=16 V, batch 32,768, flat solver, RTX 4090
 # (BatchLAS perf_steqr, "What ships" table: 450.9 us per call).
 PAGES_BASELINE = 32768 / 450.9e-6
+# DRAM bytes (read + write) per launch measured by ncu for a kernel variant,
+# keyed by bstq_describe()'s text; a changed kernel no longer matches and
+# reports null (profiles/lane_f32_n16_V_batch32768.md).
+NCU_TRAFFIC = {
+    "lane<f32,16,V,hybrid,flat> tpb=224 grid=147 smem=143360 regs=255 work=131072": 4.72e6,
+}
 SM_FP32_LANES = 128     # FP32 FMA lanes per SM (Blackwell SM)
 SM_FP64_LANES = 2       # FP64 FMA lanes per SM on GB300 (1.25 TFLOP/s nominal)
+
+
+def aggregate(local_ms, local_problems, world, dist=None, device="cpu"):
+    """Whole-job numbers over ranks: the slowest rank's time (max) and the
+    problems all ranks solved (sum).  world == 1 needs no process group."""
+    if world == 1:
+        return float(local_ms), int(local_problems)
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    c = torch.tensor([float(local_problems)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(round(c.item()))
+
+
+def rank_seed(rank):
+    """Each rank solves its own batch (weak scaling): seed = rank."""
+    return int(rank)
 
 
 def wl_name(w):
@@ -136,12 +160,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def time_workload(w, steps, warmup, dist_barrier, flush, stream, **params):
-    """Device-side timing of `steps` solves; returns (ms list, counts, extra)."""
+def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, **params):
+    """Device-side timing of `steps` solves; returns (ms list, d, e, kernel)."""
     import torch
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
     dt = np.float32 if w["dtype"] == "float32" else np.float64
-    d, e = inputs.normal_problems(w["n"], w["batch"], dt, seed=0)
+    d, e = inputs.normal_problems(w["n"], w["batch"], dt, seed=seed)
     dev = torch.device("cuda")
     d0 = torch.from_numpy(d).to(dev)
     eg = torch.from_numpy(e).to(dev)
@@ -314,13 +338,10 @@ def main():
         return 0
 
     with ClockSampler(local) as clk:
-        ms, d, e, desc = time_workload(HEADLINE, args.steps, args.warmup, barrier, flush, stream)
+        ms, d, e, desc = time_workload(HEADLINE, args.steps, args.warmup, barrier, flush, stream,
+                                       seed=rank_seed(rank))
     clocks = clk.summary()
-    mean_ms = statistics.mean(ms)
-    if world > 1:
-        t = torch.tensor([mean_ms], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms, total_problems = aggregate(statistics.mean(ms), HEADLINE["batch"], world, tdist, "cuda")
 
     e2e_ms, h2d, d2h = time_e2e(HEADLINE, max(3, args.steps // 4), 2, stream)
 
@@ -338,11 +359,13 @@ def main():
                                      "gflop": fl / 1e9, "mb": by / 1e6}
 
     if rank != 0:
+        if world > 1:
+            tdist.destroy_process_group()
         return 0
     counts = oracle_counts(HEADLINE, d, e)
     flops, bytes_ = algorithmic(HEADLINE, counts)
     t = mean_ms / 1e3
-    value = HEADLINE["batch"] * world / t
+    value = total_problems / t
     achieved = flops / t
     roof_t = max(flops / fp32_peak, bytes_ / hbm_peak)
     line = {
@@ -354,7 +377,7 @@ def main():
                    "l2": "flushed between steps (256 MiB write)", "kernel": desc,
                    "sweep_budget": "30 per eigenvalue"},
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": fp32_peak / 1e12,
-                     "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": NCU_TRAFFIC.get(desc),
                      "roofline_fraction": roof_t / t,
                      "peak_source": f"derived: {sms} SMs x {SM_FP32_LANES} FP32 lanes x 2 x {sm_max_mhz:.0f} MHz",
                      "algorithmic_gflop_per_launch": flops / 1e9, "algorithmic_mb_per_launch": bytes_ / 1e6,
