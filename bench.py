@@ -291,6 +291,7 @@ def main():
     ap.add_argument("--no-companions", action="store_true")
     ap.add_argument("--sched", type=int, default=0, help="0 auto, 1 flat, 2 nested (with --only)")
     ap.add_argument("--qstore", type=int, default=0, help="Q storage policy (with --only)")
+    ap.add_argument("--kernel", type=int, default=0, help="kernel family 1 static, 2 dynamic (with --only)")
     ap.add_argument("--only", default=None,
                     help="time one workload 'dtype:n:V|N[:batch]' and print its line (profiling aid)")
     args = ap.parse_args()
@@ -331,7 +332,7 @@ def main():
         w = dict(dtype={"f32": "float32", "f64": "float64"}.get(parts[0], parts[0]), n=int(parts[1]),
                  jobz=parts[2].upper() == "V", batch=int(parts[3]) if len(parts) > 3 else 32768)
         wm, wd, we, wdesc = time_workload(w, args.steps, args.warmup, barrier, flush, stream,
-                                          scheduler=args.sched, qstore=args.qstore)
+                                          scheduler=args.sched, qstore=args.qstore, kernel=args.kernel)
         t = statistics.mean(wm) / 1e3
         print(json.dumps({"workload": wl_name(w), "ms": t * 1e3, "problems_per_s": w["batch"] / t,
                           "kernel": wdesc}))

@@ -67,7 +67,9 @@ typedef enum {
     BSTQ_QSTORE_REGISTERS = 1, /* whole Q in registers (small n)         */
     BSTQ_QSTORE_SHARED = 2,    /* per-lane columns in shared memory      */
     BSTQ_QSTORE_GLOBAL = 3,    /* per-lane columns in `work` (L1/L2)     */
-    BSTQ_QSTORE_HYBRID = 4     /* 8 rows in registers, rest in shared    */
+    BSTQ_QSTORE_HYBRID = 4,    /* 8 rows in registers, rest in shared    */
+    BSTQ_QSTORE_SPLIT = 5      /* float, n <= 16: separate warps apply the
+                                  rotations to Q held in their registers */
 } bstq_qstore;
 
 /* Options; an all-zero struct means the defaults. */
@@ -79,7 +81,18 @@ typedef struct {
     int qstore;            /* bstq_qstore                                    */
     int threads_per_block; /* 0 = chosen by the library; else a multiple of
                               32 in [32, 1024]                               */
+    int kernel;            /* bstq_kernel: 0 = chosen per (dtype, jobz, n)   */
 } bstq_params;
+
+/* Kernel family.  STATIC: d and e in registers, the chase unrolled over
+ * compile-time positions (Q in registers, shared or global memory per
+ * qstore).  DYNAMIC: d and e in shared memory, each lane chases its own
+ * positions in a rolled loop, Q in global scratch (qstore ignored). */
+typedef enum {
+    BSTQ_KERNEL_AUTO = 0,
+    BSTQ_KERNEL_STATIC = 1,
+    BSTQ_KERNEL_DYNAMIC = 2
+} bstq_kernel;
 
 #define BSTQ_ERR_CUDA 1
 #define BSTQ_ERR_NODEVICE 2

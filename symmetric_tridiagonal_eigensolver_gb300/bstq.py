@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libbstq.so")
 F32, F64 = 0, 1
 JOBZ_N, JOBZ_V = 0, 1
 SCHED_AUTO, SCHED_FLAT, SCHED_NESTED = 0, 1, 2
-QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID = 0, 1, 2, 3, 4
+QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID, QSTORE_SPLIT = 0, 1, 2, 3, 4, 5
+KERNEL_AUTO, KERNEL_STATIC, KERNEL_DYNAMIC = 0, 1, 2
 ERR_CUDA, ERR_NODEVICE = 1, 2
 MAX_N = 32
 
@@ -32,7 +33,7 @@ class Params(ctypes.Structure):
     """bstq_params; all-zero means the defaults."""
     _fields_ = [("no_sort", ctypes.c_int), ("max_sweeps_per_n", ctypes.c_int),
                 ("scheduler", ctypes.c_int), ("qstore", ctypes.c_int),
-                ("threads_per_block", ctypes.c_int)]
+                ("threads_per_block", ctypes.c_int), ("kernel", ctypes.c_int)]
 
 
 class BstqError(RuntimeError):
@@ -89,9 +90,9 @@ def load(path: str = LIB_PATH):
         return lib
 
 
-def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0):
+def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0, kernel=0):
     return Params(int(bool(no_sort)), int(max_sweeps_per_n), int(scheduler), int(qstore),
-                  int(threads_per_block))
+                  int(threads_per_block), int(kernel))
 
 
 def _dtype_code(dt) -> int:

@@ -9,7 +9,7 @@
 #include <mutex>
 
 #include "../../include/bstq.h"
-#include "bstq_lane.cuh"
+#include "bstq_split.cuh"
 #include "bstq_registry.h"
 
 namespace bstq {
@@ -75,7 +75,7 @@ bool dev_info(DevInfo &out)
     return true;
 }
 
-const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched)
+const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched, int family)
 {
     typedef const KernelEntry *(*Lister)(int *);
 #define BSTQ_LISTER(name) entries_##name,
@@ -86,7 +86,7 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched)
         const KernelEntry *t = l(&cnt);
         for (int i = 0; i < cnt; ++i)
             if (t[i].dtype == dtype && t[i].jobz == jobz && t[i].nm == nm &&
-                t[i].qs == (jobz ? qs : 0) && t[i].sched == sched)
+                t[i].qs == (jobz ? qs : 0) && t[i].sched == sched && t[i].family == family)
                 return &t[i];
     }
     return nullptr;
@@ -116,6 +116,20 @@ int memory_rows(int dtype, int nm, int qs)
 // Default scheduler per (dtype, chunk): flat lockstep.
 int default_sched(int, int) { return SCHED_FLAT; }
 
+// Default kernel family (static positions in registers, or dynamic
+// positions with d and e in shared memory), per (dtype, jobz, n) from
+// measurement on GB300 (batch 32768/65536): float n <= 16 runs faster with
+// the static kernels (f32 n=16 V 0.167 vs 0.298 ms, N 0.088 vs 0.131 ms);
+// double, and float n > 16, with the dynamic ones (f64 n=12 V 1.27 vs
+// 1.44 ms, f64 n=32 V 14.8 vs 21.7 ms, f32 n=32 V 2.48 vs 3.43 ms).
+int default_family(int dtype, int jobz, int nm)
+{
+    (void)jobz;
+    if (dtype == 0)
+        return nm <= 16 ? FAMILY_STATIC : FAMILY_DYNAMIC;
+    return nm <= 8 ? FAMILY_STATIC : FAMILY_DYNAMIC;
+}
+
 int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p)
 {
     if (dtype != BSTQ_F32 && dtype != BSTQ_F64)
@@ -133,7 +147,9 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
             return -10;
         if (p->scheduler < 0 || p->scheduler > 2)
             return -10;
-        if (p->qstore < 0 || p->qstore > 4)
+        if (p->qstore < 0 || p->qstore > 5)
+            return -10;
+        if (p->kernel < 0 || p->kernel > 2)
             return -10;
         if (p->threads_per_block != 0 &&
             (p->threads_per_block < 32 || p->threads_per_block > 1024 || p->threads_per_block % 32))
@@ -155,9 +171,12 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
             nm = v;
             break;
         }
-    const int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm)) : 0;
+    const int family = (p && p->kernel) ? p->kernel : default_family(dtype, jobz, nm);
+    int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm)) : 0;
+    if (family == FAMILY_DYNAMIC && jobz)
+        qs = QS_GLOBAL;  // the dynamic kernels keep Q in global scratch
     const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
-    pl.k = find_entry(dtype, jobz, nm, qs, sched);
+    pl.k = find_entry(dtype, jobz, nm, qs, sched, family);
     if (!pl.k)
         return -10;
     cudaFuncAttributes fa;
@@ -165,12 +184,36 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         cudaGetLastError();
         return BSTQ_ERR_NODEVICE;
     }
+    if (qs == QS_SPLIT) {
+        // fixed shape: kSplitPairs chase warps + kSplitPairs Q warps per block,
+        // 32 * kSplitPairs problems per block; shared memory as SplitSmem<nm>
+        const int P = kSplitPairs;
+        const int rr = nm <= 12 ? nm : 12;
+        size_t off = 2ull * nm * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
+                     size_t(P) * 32 * (16 + nm);
+        off = (off + 15) / 16 * 16;
+        pl.smem = off + size_t(P) * 32 * nm * (nm - rr) * 4;
+        pl.tpb = 64 * P;
+        if (p && p->threads_per_block && p->threads_per_block != pl.tpb)
+            return -10;
+        if (fa.maxThreadsPerBlock < pl.tpb || pl.smem > (size_t)di.max_smem_block)
+            return -10;
+        pl.grid = batch > 0 ? (batch + 32 * P - 1) / (32 * P) : 0;
+        pl.qwork_bytes = 0;
+        pl.work_bytes = align256(size_t(batch) * 4);
+        if (pl.work_bytes == 0)
+            pl.work_bytes = 256;
+        return 0;
+    }
     const size_t elem = dtype ? 8 : 4;
     const size_t mem_per_thread = jobz ? size_t(nm) * memory_rows(dtype, nm, qs) * elem : 0;
     // shared memory per thread: the memory rows of Q (shared / hybrid) and
     // the mirror of d and e the settle step reads at dynamic positions
     const size_t smem_per_thread =
-        ((qs == QS_SMEM || qs == QS_HYBRID) ? mem_per_thread : 0) + 2 * size_t(nm) * elem;
+        ((family == FAMILY_STATIC && (qs == QS_SMEM || qs == QS_HYBRID)) ? mem_per_thread : 0) +
+        2 * size_t(nm) * elem +
+        // column scales of the factored double eigenvector update
+        ((family == FAMILY_DYNAMIC && dtype == BSTQ_F64 && jobz) ? 2 * size_t(nm) * elem : 0);
     // Threads an SM can hold for this kernel.
     const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
     int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);
@@ -222,6 +265,7 @@ const char *qs_name(int qs)
     case QS_SMEM: return "shared";
     case QS_GLOBAL: return "global";
     case QS_HYBRID: return "hybrid";
+    case QS_SPLIT: return "split";
     default: return "none";
     }
 }
@@ -384,8 +428,9 @@ extern "C" int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t ba
             regs = fa.numRegs;
         else
             cudaGetLastError();
-        snprintf(buf, len, "lane<%s,%d,%s,%s,%s> tpb=%d grid=%lld smem=%zu regs=%d work=%zu",
-                 dtype ? "f64" : "f32", pl.k->nm, jobz ? "V" : "N", jobz ? qs_name(pl.k->qs) : "none",
+        snprintf(buf, len, "%s<%s,%d,%s,%s,%s> tpb=%d grid=%lld smem=%zu regs=%d work=%zu",
+                 pl.k->family == FAMILY_DYNAMIC ? "dyn" : "lane", dtype ? "f64" : "f32", pl.k->nm,
+                 jobz ? "V" : "N", jobz ? qs_name(pl.k->qs) : "none",
                  pl.k->sched == SCHED_FLAT ? "flat" : "nested", pl.tpb, pl.grid, pl.smem, regs, pl.work_bytes);
     }
     return 0;

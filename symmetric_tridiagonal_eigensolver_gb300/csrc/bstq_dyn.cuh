@@ -1,0 +1,599 @@
+// Lane-per-problem steqr kernel, dynamic-position form.
+//
+// One CUDA thread owns one problem of size n <= NM, as in bstq_lane.cuh, but
+// d and e live in shared memory (entry i of the lane's d at sd[i * blockDim],
+// of e at se[i * blockDim]: the lanes of a warp hit consecutive words whatever
+// index each one is at, so no access conflicts) and every lane chases its own
+// positions.  A sweep of L rotations is L steps of a rolled loop; the warp
+// runs max(L) steps per pass (flat scheduler) and a lane past its own sweep
+// sits the rest out.  Compared with the static-position kernel there is no
+// union of position ranges to pay for and the loop body is small.
+//
+// The per-problem operations are those of the BatchLAS page "algo_steqr"
+// (deflation, scaling, copysign shift, lartg + EXP bulge chase, direct 2x2
+// solve, eigenvector accumulation, ascending sort) with QR blocks mirrored at
+// load as in bstq_lane.cuh ("perf_steqr", direction unification), and the
+// schedulers of "perf_steqr", section "Lockstep flat solver".
+#pragma once
+
+#include "bstq_lane.cuh"
+
+namespace bstq {
+
+// Q columns in memory (global scratch or shared), one 16-byte vector per
+// group of rows, vector g of column k of thread t at base[(k*G + g)*stride+t].
+template <typename T, int NM>
+struct DynQ {
+    using Tr = El<T>;
+    using E = typename Tr::E;
+    static constexpr int RPE = Tr::RPE;
+    static constexpr int W = 16 / (int)sizeof(T);
+    static constexpr int NR = ((NM + W - 1) / W) * W;  // stored rows
+    static constexpr int NE = NR / RPE;
+    static constexpr int G = NE / 2;
+    struct V16 {
+        E a, b;
+    };
+    V16 *base;
+    int stride;
+
+    __device__ __forceinline__ void load(int k, E (&x)[NE]) const
+    {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const V16 v = base[(k * G + g) * stride];
+            x[2 * g] = v.a;
+            x[2 * g + 1] = v.b;
+        }
+    }
+    __device__ __forceinline__ void store(int k, const E (&x)[NE]) const
+    {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
+    }
+    __device__ __forceinline__ void init_col(int s, int row_of_one) const
+    {
+        E x[NE];
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+            x[j] = Tr::unit(row_of_one, j * RPE);
+        store(s, x);
+    }
+};
+
+// double eigenvectors are accumulated in factored form Q = Qt diag(delta)
+// (fast Givens, after Gentleman): a rotation then costs two FMAs per row
+// instead of two multiplies and two FMAs, plus a dozen scalar operations for
+// the column scales; delta and its inverse live in shared memory.
+template <typename T, bool WANTZ>
+constexpr bool dyn_fastq()
+{
+    return WANTZ && sizeof(T) == 8;
+}
+
+template <typename T, int NM, bool WANTZ>
+struct DynLane {
+    using C_ = Consts<T>;
+    using Q_ = DynQ<T, NM>;
+    using E = typename Q_::E;
+    static constexpr int NE = Q_::NE;
+    static constexpr bool FASTQ = dyn_fastq<T, WANTZ>();
+
+    T *sd, *se;  // this lane's d and e in shared memory
+    T *sdl, *sil;  // column scales delta_j and 1/delta_j (FASTQ)
+    int ms;      // their stride (blockDim.x)
+    T da, ia;    // scale and inverse scale of the carried column C (FASTQ)
+    int n, status, info;
+    unsigned zmask, revmask;
+    bool inblock;
+    int bnext, lb, le, lo;
+    int iscale;
+    T pre, sc, aeff, anorm;
+    int jtot, budget;
+    int task, m;
+    T f, g;        // running pair
+    T cs2, sn2;    // pending 2x2 rotation
+    // pass state
+    int L, C;      // steps of the current task, current position
+    T a_reg, b_reg;  // d_C and e_{C-1} as updated by the previous step
+    Q_ q;
+    E cur[NE];     // Q column C (the column shared with the next rotation)
+
+    __device__ __forceinline__ T D(int i) const { return sd[i * ms]; }
+    __device__ __forceinline__ T Ev(int i) const { return se[i * ms]; }
+    __device__ __forceinline__ void setD(int i, T v) { sd[i * ms] = v; }
+    __device__ __forceinline__ void setE(int i, T v) { se[i * ms] = v; }
+
+    __device__ __forceinline__ int phys(int s) const
+    {
+        int a = block_lo(zmask, s), b = block_hi(zmask, s);
+        return ((revmask >> a) & 1u) ? (a + b - s) : s;
+    }
+
+    __device__ __forceinline__ void scale_factors(T an, int &isc, T &pr, T &s, T &ae) const
+    {
+        isc = 0;
+        pr = T(1);
+        s = T(1);
+        ae = an;
+        if (an > C_::ssfmax) {
+            isc = 1;
+            s = C_::ssfmax / an;
+        } else if (an < C_::ssfmin) {
+            isc = 2;
+            if (an < C_::safmin) {
+                pr = C_::prescale;
+                ae = an * pr;
+            }
+            s = C_::ssfmin / ae;
+        }
+    }
+
+    __device__ __forceinline__ T block_norm(int a, int b) const
+    {
+        T an = T(0);
+        for (int i = a; i <= b; ++i)
+            an = fmax(an, dabs(D(i)));
+        for (int i = a; i < b; ++i)
+            an = fmax(an, dabs(Ev(i)));
+        return an;
+    }
+
+    __device__ void load(const KParams &p, long long b, bool live)
+    {
+        n = p.n;
+        budget = p.budget;
+        jtot = 0;
+        task = TASK_NONE;
+        inblock = false;
+        bnext = 0;
+        lb = le = lo = m = 0;
+        info = 0;
+        revmask = 0;
+        iscale = 0;
+        pre = sc = aeff = anorm = T(1);
+        f = g = cs2 = sn2 = a_reg = b_reg = T(0);
+        L = 0;
+        C = 0;
+        if (!live) {
+            status = ST_DEAD;
+            zmask = ~0u;
+            return;
+        }
+        const T *dg = reinterpret_cast<const T *>(p.d) + b * n;
+        const T *eg = reinterpret_cast<const T *>(p.e) + b * (n - 1);
+        bool bad = false;
+        zmask = 0;
+        for (int i = 0; i < n; ++i) {
+            const T di = dg[i];
+            const T ei = i < n - 1 ? eg[i] : T(0);
+            setD(i, di);
+            setE(i, ei);
+            bad |= !isfinite(di) || !isfinite(ei);
+            if (i >= n - 1 || ei == T(0))
+                zmask |= 1u << i;
+        }
+        zmask |= n < 32 ? (~0u << n) : 0u;
+        status = bad ? ST_BAD : ST_RUN;
+        if (bad)
+            return;
+        for (int a = 0; a < n;) {
+            const int z = block_hi(zmask, a);
+            if (z > a) {
+                const T an = block_norm(a, z);
+                if (an > T(0)) {
+                    int isc;
+                    T pr, s, ae;
+                    scale_factors(an, isc, pr, s, ae);
+                    T x = D(a), y = D(z);
+                    if (isc) {
+                        x = (x * pr) * s;
+                        y = (y * pr) * s;
+                    }
+                    if (dabs(x) > dabs(y))
+                        revmask |= 1u << a;
+                }
+            }
+            a = z + 1;
+        }
+        if (revmask) {
+            for (int s = 0; s < n; ++s) {
+                const int ps = phys(s);
+                setD(s, dg[ps]);
+                if (s < n - 1 && !((zmask >> s) & 1u)) {
+                    const int pn = phys(s + 1);
+                    setE(s, eg[ps < pn ? ps : pn]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void scale_range(T f1, T f2, bool with_e)
+    {
+        for (int i = lb; i <= le; ++i)
+            setD(i, (D(i) * f1) * f2);
+        if (with_e)
+            for (int i = lb; i < le; ++i)
+                setE(i, (Ev(i) * f1) * f2);
+    }
+
+    __device__ __forceinline__ void unscale_block(bool with_e)
+    {
+        if (iscale == 0)
+            return;
+        T us, up = T(1);
+        if (iscale == 1) {
+            us = anorm / C_::ssfmax;
+        } else {
+            us = aeff / C_::ssfmin;
+            up = T(1) / pre;
+        }
+        scale_range(us, up, with_e);
+    }
+
+    __device__ __forceinline__ void close_block()
+    {
+        unscale_block(false);
+        inblock = false;
+    }
+
+    // One settle event; true while the lane still needs settling.
+    __device__ bool settle_step()
+    {
+        if (!inblock) {
+            if (bnext >= n) {
+                status = ST_DONE;
+                return false;
+            }
+            lb = bnext;
+            le = block_hi(zmask, lb);
+            bnext = le + 1;
+            if (le == lb)
+                return true;
+            anorm = block_norm(lb, le);
+            if (anorm == T(0))
+                return true;
+            scale_factors(anorm, iscale, pre, sc, aeff);
+            if (iscale)
+                scale_range(pre, sc, true);
+            lo = lb;
+            inblock = true;
+        }
+        // first negligible off-diagonal from lo (page "algo_steqr")
+        int mm = le;
+        T dcur = D(lo);
+        for (int i = lo; i < le; ++i) {
+            const T dn = D(i + 1);
+            const T ev = Ev(i);
+            bool neg;
+            if constexpr (sizeof(T) == 8) {
+                // Exponent bounds first (integer pipe).  With k the biased
+                // exponent field, 2^(k-1023) <= |x| < 2^(k-1022) (the upper
+                // bound holds for zero and subnormals too), so
+                // e^2 >= 2^(2 k_e - 2046), eps^2 |d_i d_i+1| < 2^(k_1 + k_2 - 2150)
+                // and safmin = 2^-1022.  When 2 k_e >= k_1 + k_2 - 99 and
+                // 2 k_e >= 1037, e^2 exceeds each term of the threshold by a
+                // factor of 8 or more, so the off-diagonal is certainly not
+                // negligible and the FP64 test is skipped.  (Scaled inputs
+                // are finite here.)
+                const int ke = (__double2hiint(ev) >> 20) & 0x7ff;
+                const int k1 = (__double2hiint(dcur) >> 20) & 0x7ff;
+                const int k2 = (__double2hiint(dn) >> 20) & 0x7ff;
+                const bool clear = (2 * ke > k1 + k2 - 100) && (2 * ke > 1036);
+                neg = false;
+                if (!clear) {
+                    const T ae = dabs(ev);
+                    const T tst = ae * ae;
+                    const T thr = fma(C_::eps2 * dabs(dcur), dabs(dn), C_::safmin);
+                    // non-negative doubles order as their bit patterns
+                    neg = __double_as_longlong(tst) <= __double_as_longlong(thr);
+                }
+            } else {
+                const T ae = dabs(ev);
+                const T tst = ae * ae;
+                const T thr = fma(C_::eps2 * dabs(dcur), dabs(dn), C_::safmin);
+                neg = tst <= thr;
+            }
+            if (neg) {
+                mm = i;
+                break;
+            }
+            dcur = dn;
+        }
+        if (mm < le)
+            setE(mm, T(0));
+        if (mm == lo) {
+            ++lo;
+            if (lo > le)
+                close_block();
+            return true;
+        }
+        const T d1 = D(lo), d2 = D(lo + 1), e1 = Ev(lo);
+        if (mm == lo + 1) {
+            solve2x2(d1, e1, d2, cs2, sn2);
+            task = TASK_2X2;
+            m = lo + 1;
+            return false;
+        }
+        if (jtot == budget) {
+            unscale_block(true);
+            int cnt = 0;
+            for (int i = 0; i < n - 1; ++i)
+                cnt += Ev(i) != T(0) ? 1 : 0;
+            info = cnt;
+            status = ST_FAIL;
+            return false;
+        }
+        ++jtot;
+        const T mu = wilkinson_shift(d1, d2, e1);
+        f = D(mm) - mu;
+        g = Ev(mm - 1);
+        m = mm;
+        task = TASK_SWEEP;
+        return false;
+    }
+
+    __device__ __forceinline__ bool has_task() const { return status == ST_RUN && task != TASK_NONE; }
+
+    __device__ __forceinline__ void begin_pass()
+    {
+        if (!has_task()) {
+            L = 0;
+            return;
+        }
+        C = m;
+        L = m - lo;  // 1 for a 2x2 task
+        a_reg = D(C);
+        b_reg = Ev(C - 1);
+        if constexpr (WANTZ)
+            q.load(C, cur);
+        if constexpr (FASTQ) {
+            da = sdl[C * ms];
+            ia = sil[C * ms];
+        }
+    }
+
+    // Rotation k of the lane's task, on the pair (C, C-1).
+    __device__ __forceinline__ void step(int k)
+    {
+        const bool sweep = task == TASK_SWEEP;
+        T cs, sn, r = T(0);
+        if (sweep) {
+            if constexpr (sizeof(T) == 8)
+                lartg_fast(f, g, cs, sn, r);
+            else
+                lartg(f, g, cs, sn, r);
+        } else {
+            cs = cs2;
+            sn = sn2;
+        }
+        const T a = a_reg, b = b_reg, cc = D(C - 1);
+        // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP)
+        const T p1 = fma(cs, a, sn * b);
+        const T p2 = fma(cs, b, sn * cc);
+        const T dn = fma(cs, p1, sn * p2);
+        T en = fma(cs, p2, -sn * p1);
+        const T dm = (a + cc) - dn;
+        setD(C, dn);
+        if (sweep && k > 0)
+            setE(C, r);
+        if (!sweep)
+            en = T(0);
+        if (C - 1 > lo) {
+            const T eo = Ev(C - 2);
+            g = sn * eo;  // new bulge
+            b_reg = cs * eo;
+            f = en;
+            a_reg = dm;
+        } else {
+            setD(C - 1, dm);
+            setE(C - 1, en);
+        }
+        if constexpr (FASTQ) {
+            // q_C = da x, q_{C-1} = db y.  Form 1 (|cs| >= |sn|):
+            //   x' = x + P y, y' = y - M x, da' = cs da, db' = cs db;
+            // form 2 (|sn| > |cs|), columns exchange their roles:
+            //   x' = y + M x, y' = x - P y, da' = sn db, db' = -sn da;
+            // with t = sn/cs (form 1) or cs/sn (form 2), P = t db/da,
+            // M = t da/db.  Either way Qt' diag(delta') = Qt diag(delta) G.
+            E nx[NE];
+            q.load(C - 1, nx);
+            const T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
+            const bool f1 = (__double_as_longlong(cs) & 0x7fffffffffffffffll) >=
+                            (__double_as_longlong(sn) & 0x7fffffffffffffffll);
+            const T rp = rcp_nr(f1 ? cs : sn);
+            const T t = (f1 ? sn : cs) * rp;
+            const T P = t * (db * ia), M = t * (da * ib);
+            const T c1 = f1 ? P : M, c2 = f1 ? -M : -P;
+#pragma unroll
+            for (int j = 0; j < NE; ++j) {
+                const E u = cur[j], v = nx[j];
+                const E s1 = f1 ? v : u, s2 = f1 ? u : v;
+                cur[j] = fma(c1, s1, s2);
+                nx[j] = fma(c2, s2, s1);
+            }
+            const T da2 = (f1 ? cs : sn) * (f1 ? da : db);
+            const T db2 = (f1 ? cs : -sn) * (f1 ? db : da);
+            const T ia2 = (f1 ? ia : ib) * rp;
+            const T ib2 = (f1 ? ib : -ia) * rp;
+            q.store(C, cur);
+            sdl[C * ms] = da2;
+            sil[C * ms] = ia2;
+            if (C - 1 > lo) {
+#pragma unroll
+                for (int j = 0; j < NE; ++j)
+                    cur[j] = nx[j];
+                da = db2;
+                ia = ib2;
+            } else {
+                q.store(C - 1, nx);
+                sdl[(C - 1) * ms] = db2;
+                sil[(C - 1) * ms] = ib2;
+            }
+        } else if constexpr (WANTZ) {
+            E nx[NE];
+            q.load(C - 1, nx);
+            const typename El<T>::R rr = El<T>::make(cs, sn);
+#pragma unroll
+            for (int j = 0; j < NE; ++j)
+                El<T>::rot(cur[j], nx[j], rr);
+            q.store(C, cur);
+            if (C - 1 > lo) {
+#pragma unroll
+                for (int j = 0; j < NE; ++j)
+                    cur[j] = nx[j];
+            } else {
+                q.store(C - 1, nx);
+            }
+        }
+        --C;
+    }
+
+    __device__ __forceinline__ void post_pass()
+    {
+        if (task == TASK_2X2) {
+            lo += 2;
+            if (lo > le)
+                close_block();
+        }
+        task = TASK_NONE;
+        L = 0;
+    }
+};
+
+template <typename T, int NM, bool WANTZ, int SCHED>
+__global__ void dyn_kernel(KParams p)
+{
+    extern __shared__ uint4 smem_raw[];
+    using LaneT = DynLane<T, NM, WANTZ>;
+    const int tpb = blockDim.x;
+    const long long b = (long long)blockIdx.x * tpb + threadIdx.x;
+    const bool live = b < p.batch;
+
+    LaneT L;
+    L.ms = tpb;
+    L.sd = reinterpret_cast<T *>(smem_raw) + threadIdx.x;
+    L.se = L.sd + NM * tpb;
+    L.sdl = L.se + NM * tpb;
+    L.sil = L.sdl + NM * tpb;
+    L.da = L.ia = T(1);
+    if constexpr (WANTZ) {
+        // Q scratch in global memory: per block NM columns x G vectors x tpb
+        constexpr int G = DynQ<T, NM>::G;
+        L.q.base = reinterpret_cast<typename DynQ<T, NM>::V16 *>(p.qwork) +
+                   ((long long)blockIdx.x * NM * G * tpb + threadIdx.x);
+        L.q.stride = tpb;
+    }
+    L.load(p, b, live);
+    if constexpr (WANTZ) {
+        if (L.status == ST_RUN)
+            for (int s = 0; s < NM; ++s) {
+                L.q.init_col(s, s < L.n ? L.phys(s) : s);
+                if constexpr (LaneT::FASTQ) {
+                    L.sdl[s * tpb] = T(1);
+                    L.sil[s * tpb] = T(1);
+                }
+            }
+    }
+
+    if (SCHED == SCHED_FLAT) {
+        for (;;) {
+            bool need = (L.status == ST_RUN) && (L.task == TASK_NONE);
+            while (__any_sync(FULL, need)) {
+                if (need)
+                    need = L.settle_step();
+            }
+            const bool has = L.has_task();
+            if (!__any_sync(FULL, has))
+                break;
+            L.begin_pass();
+            const int steps = __reduce_max_sync(FULL, L.L);
+            for (int k = 0; k < steps; ++k)
+                if (k < L.L)
+                    L.step(k);
+            if (has)
+                L.post_pass();
+        }
+    } else {
+        while (L.status == ST_RUN) {
+            if (L.task == TASK_NONE) {
+                L.settle_step();
+                continue;
+            }
+            L.begin_pass();
+            for (int k = 0; k < L.L; ++k)
+                L.step(k);
+            L.post_pass();
+        }
+    }
+
+    if (!live)
+        return;
+    const int n = L.n;
+    T *dout = reinterpret_cast<T *>(p.d) + b * n;
+    T *qout = WANTZ ? reinterpret_cast<T *>(p.Q) + b * (long long)n * n : nullptr;
+    if (L.status == ST_BAD) {
+        const T nan = T(__int_as_float(0x7fffffff));
+        for (int i = 0; i < n; ++i)
+            dout[i] = nan;
+        if (WANTZ)
+            for (int i = 0; i < n * n; ++i)
+                qout[i] = nan;
+        p.info[b] = -1;
+        return;
+    }
+    // eigenvalues into registers for the ranking
+    T dv[NM];
+    int ph[NM], pos[NM];
+    const bool sorted = p.sort && L.status == ST_DONE;
+#pragma unroll
+    for (int s = 0; s < NM; ++s) {
+        dv[s] = s < n ? L.D(s) : T(0);
+        ph[s] = s < n ? L.phys(s) : s;
+        pos[s] = sorted ? 0 : ph[s];
+    }
+    if (sorted) {
+#pragma unroll
+        for (int s = 0; s < NM; ++s) {
+#pragma unroll
+            for (int t = s + 1; t < NM; ++t) {
+                if (t < n) {
+                    const bool lt = (dv[t] < dv[s]) || (dv[t] == dv[s] && ph[t] < ph[s]);
+                    pos[s] += lt ? 1 : 0;
+                    pos[t] += lt ? 0 : 1;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < NM; ++s)
+        if (s < n)
+            dout[pos[s]] = dv[s];
+    if constexpr (WANTZ) {
+        using Q_ = DynQ<T, NM>;
+        for (int s = 0; s < n; ++s) {
+            typename Q_::E x[Q_::NE];
+            L.q.load(s, x);
+            T col[Q_::NR];
+#pragma unroll
+            for (int j = 0; j < Q_::NE; ++j)
+                El<T>::get(x[j], &col[j * Q_::RPE]);
+            int ps = 0;
+#pragma unroll
+            for (int t = 0; t < NM; ++t)
+                ps = (t == s) ? pos[t] : ps;
+            T scale = T(1);
+            if constexpr (LaneT::FASTQ)
+                scale = L.sdl[s * tpb];  // Q = Qt diag(delta)
+            T *qc = qout + (long long)ps * n;
+#pragma unroll
+            for (int r = 0; r < NM; ++r)
+                if (r < n)
+                    qc[r] = LaneT::FASTQ ? col[r] * scale : col[r];
+        }
+    }
+    p.info[b] = (L.status == ST_FAIL) ? L.info : 0;
+}
+
+}  // namespace bstq

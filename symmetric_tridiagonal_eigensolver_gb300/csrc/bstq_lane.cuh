@@ -32,7 +32,7 @@
 
 namespace bstq {
 
-enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3, QS_HYBRID = 4 };
+enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3, QS_HYBRID = 4, QS_SPLIT = 5 };
 enum { SCHED_FLAT = 1, SCHED_NESTED = 2 };
 enum { ST_RUN = 0, ST_DONE = 1, ST_FAIL = 2, ST_BAD = 3, ST_DEAD = 4 };
 enum { TASK_NONE = 0, TASK_SWEEP = 1, TASK_2X2 = 2 };

@@ -174,7 +174,33 @@ __device__ __forceinline__ void lartg(float f, float g, float &c, float &s, floa
     r = z ? f : r;
 }
 
+// double, FP64-lean: r2 = f^2 + g^2 directly while its exponent (read on the
+// integer pipe) is comfortably inside the normal range, else (a rare,
+// divergent branch) the scaled form below.
+__device__ __forceinline__ void lartg_scaled(double f, double g, double &c, double &s, double &r);
+
+__device__ __forceinline__ void lartg_fast(double f, double g, double &c, double &s, double &r)
+{
+    const double r2 = fma(f, f, g * g);
+    const int ex = (__double2hiint(r2) >> 20) & 0x7ff;
+    const double y = rsqrt_nr(r2);
+    c = f * y;
+    s = g * y;
+    r = r2 * y;
+    if (ex < 64 || ex > 1983)
+        lartg_scaled(f, g, c, s, r);
+    const bool z = (((unsigned)__double2hiint(g) & 0x7fffffffu) | (unsigned)__double2loint(g)) == 0u;
+    c = z ? 1.0 : c;
+    s = z ? 0.0 : s;
+    r = z ? f : r;
+}
+
 __device__ __forceinline__ void lartg(double f, double g, double &c, double &s, double &r)
+{
+    lartg_scaled(f, g, c, s, r);
+}
+
+__device__ __forceinline__ void lartg_scaled(double f, double g, double &c, double &s, double &r)
 {
     const unsigned fh = (unsigned)__double2hiint(f) & 0x7fffffffu;
     const unsigned gh = (unsigned)__double2hiint(g) & 0x7fffffffu;

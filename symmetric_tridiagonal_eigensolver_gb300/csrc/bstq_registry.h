@@ -13,7 +13,10 @@ struct KernelEntry {
     int qs;      // Q storage (QS_*; 0 for jobz N)
     int sched;   // SCHED_FLAT / SCHED_NESTED
     const void *fn;
+    int family;  // FAMILY_STATIC (bstq_lane.cuh) / FAMILY_DYNAMIC (bstq_dyn.cuh)
 };
+
+enum { FAMILY_STATIC = 1, FAMILY_DYNAMIC = 2 };
 
 #define BSTQ_DECLARE_UNIT(name) const KernelEntry *entries_##name(int *count);
 BSTQ_FOR_EACH_UNIT(BSTQ_DECLARE_UNIT)

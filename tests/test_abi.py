@@ -57,9 +57,9 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     assert solve(0, 1, 8, 10, good, good, good, None, None) == -8
     mis = ctypes.c_void_p(ctypes.addressof(buf) + 2)
     assert solve(0, 1, 8, 10, mis, good, good, good, None) == -5
-    p = bstq.Params(0, 0, 9, 0, 0)
+    p = bstq.Params(0, 0, 9, 0, 0, 0)
     assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
-    p = bstq.Params(0, 0, 0, 0, 48)
+    p = bstq.Params(0, 0, 0, 0, 48, 0)
     assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
     assert lib.bstq_work_size(0, 1, 40, 10) == 0
     assert lib.bstq_solve_host(0, 1, 8, 10, None, good, good, good, good, None, None) == -5

@@ -89,3 +89,50 @@ def test_oversized_block_is_rejected_not_launched():
     with pytest.raises(bstq.BstqError) as ei:
         run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), threads_per_block=1024)
     assert ei.value.code == -10
+
+
+@pytest.mark.parametrize("dt,n", [(np.float32, 3), (np.float32, 8), (np.float32, 16), (np.float32, 21),
+                                  (np.float32, 32), (np.float64, 5), (np.float64, 12), (np.float64, 17),
+                                  (np.float64, 32)])
+@pytest.mark.parametrize("jobz", [True, False])
+def test_dynamic_family_parity_and_schedulers(dt, n, jobz):
+    """Dynamic-position kernels (d, e in shared memory, rolled chase): parity
+    with the oracle on the mixed hard cases, flat equal to nested."""
+    d, e, _, _ = inputs.mixed_problems(n, 3000, dt, seed=77 + n)
+    a = run_gpu(d, e, jobz=jobz, kernel=2, scheduler=1)
+    b = run_gpu(d, e, jobz=jobz, kernel=2, scheduler=2)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[2], b[2])
+    if jobz:
+        np.testing.assert_array_equal(a[1], b[1])
+    check_parity(d, e, *a, oracle_ref(d, e, jobz=jobz), what=f"dyn {n}")
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_dynamic_family_budget_and_poison(dt):
+    n = 14
+    d, e = inputs.normal_problems(n, 400, dt, seed=5)
+    d[3, 4] = np.nan
+    ref = oracle_ref(d, e, maxit_per_n=1)
+    lam, Q, info = run_gpu(d, e, kernel=2, max_sweeps_per_n=1)
+    assert info[3] == -1 and np.all(np.isnan(lam[3]))
+    ok = np.arange(400) != 3
+    assert np.all(info[ok] > 0) and np.mean(info[ok] == ref.info[ok]) > 0.9
+
+
+@pytest.mark.parametrize("n", [9, 12, 13, 16])
+def test_split_role_kernel(n):
+    """Chase warps record rotations, partner warps apply them to Q one pass
+    behind: same per-problem arithmetic as the static kernel, so equal
+    eigenvalues, and eigenvectors within the parity bounds."""
+    d, e, _, _ = inputs.mixed_problems(n, 3333, np.float32, seed=90 + n)
+    ref = oracle_ref(d, e)
+    a = run_gpu(d, e, qstore=5)
+    check_parity(d, e, *a, ref, what=f"split {n}")
+    b = run_gpu(d, e, qstore=4 if n > 12 else 1)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[2], b[2])
+    # poisoned and budget-exhausted problems too
+    d[7, 3] = np.inf
+    c = run_gpu(d, e, qstore=5, max_sweeps_per_n=1)
+    assert c[2][7] == -1 and np.all(np.isnan(c[1][7]))
