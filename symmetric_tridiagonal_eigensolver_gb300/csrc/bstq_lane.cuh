@@ -3,12 +3,13 @@
 // One CUDA thread owns one tridiagonal problem of size n <= NM.  d and e live
 // in registers and every access uses a compile-time index: a sweep is a pass
 // over the static chase positions C = NM-1 .. 1, entered through a jump table
-// at the warp's highest active position and left at a group boundary once no
-// lane has work below.  Each position is straight-line code: lanes for which
-// the position is outside their sweep apply the identity rotation (lartg of
-// (1, 0)) and keep d and e through selects, so a whole pass is one basic block
-// in which the eigenvector update of one position overlaps the dependency
-// chain of the next.  Dynamic positions (start of a sweep, deflation point)
+// at the group top at or above the warp's highest active position and left
+// at a group boundary once no lane has work below.  Each position is
+// straight-line code: lanes for which the position is outside their sweep
+// apply the identity rotation (lartg of (1, 0)) and keep d and e through
+// selects, so each group of positions is one basic block in which the
+// eigenvector update of one position overlaps the dependency chain of the
+// next.  Dynamic positions (start of a sweep, deflation point)
 // only occur in the settle step and are resolved with bit masks and selects.
 //
 // QR runs as QL on the mirrored block (BatchLAS page "perf_steqr", section
@@ -175,8 +176,12 @@ struct QMix {
             if (st)
                 store(col, cur);
     }
+    // The streamed column is written back unconditionally: a lane for which
+    // the position is inactive rotates by the identity and stores the values
+    // it loaded (up to the sign of a zero), and a predicated store would
+    // split the position's straight-line code.
     template <int C>
-    __device__ __forceinline__ void rot(T cs, T sn, bool st)
+    __device__ __forceinline__ void rot(T cs, T sn, bool)
     {
         const typename Tr::R r = Tr::make(cs, sn);
 #pragma unroll
@@ -188,8 +193,7 @@ struct QMix {
 #pragma unroll
             for (int j = 0; j < NEM; ++j)
                 Tr::rot(cur[j], nx[j], r);
-            if (st)
-                store(C, cur);
+            store(C, cur);
 #pragma unroll
             for (int j = 0; j < NEM; ++j)
                 cur[j] = nx[j];
@@ -269,6 +273,111 @@ __device__ __forceinline__ int block_hi(unsigned zmask, int s)
 {
     return s + __ffs(zmask >> s) - 1;
 }
+
+// ---------------------------------------------------------------------------
+// Pass entry.  A pass is left only at group boundaries (after positions
+// C with (C - 1) % KEXIT == 0) and entered only at group tops (multiples of
+// KEXIT, or NM - 1), so each group of KEXIT positions is a single basic
+// block and the compiler can overlap the eigenvector update of one position
+// with the dependency chain of the next.  Entering above the warp's highest
+// active position costs a few identity rotations; for a block that reaches
+// the end of the problem the highest position is NM - 1, already a top.
+// ---------------------------------------------------------------------------
+template <int NM, int KEXIT>
+__device__ __forceinline__ int group_top(int rhi)
+{
+    const int t = (rhi + KEXIT - 1) / KEXIT * KEXIT;
+    return t < NM - 1 ? t : NM - 1;
+}
+// switch value of a group top: NM - 1 enters at the head of the list
+template <int NM>
+__device__ __forceinline__ int group_case(int top)
+{
+    return top == NM - 1 ? 32 : top;
+}
+
+// Positions 31 .. 1 with case labels at the group tops only; S(C) expands
+// to the (compile-time guarded) code of position C.
+#define BSTQ_CASES_K4(S)                                                      \
+    case 32:                                                                  \
+        S(31) S(30) S(29)                                                     \
+    case 28:                                                                  \
+        S(28) S(27) S(26) S(25)                                               \
+    case 24:                                                                  \
+        S(24) S(23) S(22) S(21)                                               \
+    case 20:                                                                  \
+        S(20) S(19) S(18) S(17)                                               \
+    case 16:                                                                  \
+        S(16) S(15) S(14) S(13)                                               \
+    case 12:                                                                  \
+        S(12) S(11) S(10) S(9)                                                \
+    case 8:                                                                   \
+        S(8) S(7) S(6) S(5)                                                   \
+    case 4:                                                                   \
+        S(4) S(3) S(2) S(1)
+#define BSTQ_CASES_K2(S)                                                      \
+    case 32:                                                                  \
+        S(31)                                                                 \
+    case 30:                                                                  \
+        S(30) S(29)                                                           \
+    case 28:                                                                  \
+        S(28) S(27)                                                           \
+    case 26:                                                                  \
+        S(26) S(25)                                                           \
+    case 24:                                                                  \
+        S(24) S(23)                                                           \
+    case 22:                                                                  \
+        S(22) S(21)                                                           \
+    case 20:                                                                  \
+        S(20) S(19)                                                           \
+    case 18:                                                                  \
+        S(18) S(17)                                                           \
+    case 16:                                                                  \
+        S(16) S(15)                                                           \
+    case 14:                                                                  \
+        S(14) S(13)                                                           \
+    case 12:                                                                  \
+        S(12) S(11)                                                           \
+    case 10:                                                                  \
+        S(10) S(9)                                                            \
+    case 8:                                                                   \
+        S(8) S(7)                                                             \
+    case 6:                                                                   \
+        S(6) S(5)                                                             \
+    case 4:                                                                   \
+        S(4) S(3)                                                             \
+    case 2:                                                                   \
+        S(2) S(1)
+#define BSTQ_CASES_K8(S)                                                      \
+    case 32:                                                                  \
+        S(31) S(30) S(29) S(28) S(27) S(26) S(25)                             \
+    case 24:                                                                  \
+        S(24) S(23) S(22) S(21) S(20) S(19) S(18) S(17)                       \
+    case 16:                                                                  \
+        S(16) S(15) S(14) S(13) S(12) S(11) S(10) S(9)                        \
+    case 8:                                                                   \
+        S(8) S(7) S(6) S(5) S(4) S(3) S(2) S(1)
+#define BSTQ_GROUPED_SWITCH(KX, SW, S)                                        \
+    static_assert(KX == 2 || KX == 4 || KX == 8, "group size 2, 4 or 8");     \
+    if constexpr (KX == 8) {                                                  \
+        switch (SW) {                                                         \
+            BSTQ_CASES_K8(S)                                                  \
+        default:                                                              \
+            break;                                                            \
+        }                                                                     \
+    } else if constexpr (KX == 4) {                                           \
+        switch (SW) {                                                         \
+            BSTQ_CASES_K4(S)                                                  \
+        default:                                                              \
+            break;                                                            \
+        }                                                                     \
+    } else {                                                                  \
+        switch (SW) {                                                         \
+            BSTQ_CASES_K2(S)                                                  \
+        default:                                                              \
+            break;                                                            \
+        }                                                                     \
+    }
 
 // ---------------------------------------------------------------------------
 // One problem.
@@ -632,35 +741,27 @@ struct Lane {
         Q.template rot<C>(cs, sn, (m_touch >> C) & 1u);
     }
 
-    // One pass over positions rhi .. (group boundary <= rlo).
+    // One pass over positions top .. (group boundary <= rlo), where top is
+    // the first group top at or above rhi; positions above rhi are inactive
+    // in every lane (identity rotations).
     template <class QT>
     __device__ __forceinline__ void run_pass(QT &Q, int rhi, int rlo)
     {
-        Q.begin(rhi);
+        const int top = group_top<NM, KEXIT>(rhi);
+        Q.begin(top);
         int last = 0;
-        switch (rhi) {
 #define BSTQ_POS(C)                                                          \
-    case C:                                                                  \
-        if constexpr (C <= NM - 1) {                                         \
-            chase_at<C>(Q);                                                  \
-            if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                 \
-                if (C - 1 < rlo) {                                           \
-                    last = C - 1;                                            \
-                    goto pass_done;                                          \
-                }                                                            \
+    if constexpr (C <= NM - 1) {                                             \
+        chase_at<C>(Q);                                                      \
+        if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                     \
+            if (C - 1 < rlo) {                                               \
+                last = C - 1;                                                \
+                goto pass_done;                                              \
             }                                                                \
         }                                                                    \
-        [[fallthrough]];
-            BSTQ_POS(31) BSTQ_POS(30) BSTQ_POS(29) BSTQ_POS(28) BSTQ_POS(27) BSTQ_POS(26)
-            BSTQ_POS(25) BSTQ_POS(24) BSTQ_POS(23) BSTQ_POS(22) BSTQ_POS(21) BSTQ_POS(20)
-            BSTQ_POS(19) BSTQ_POS(18) BSTQ_POS(17) BSTQ_POS(16) BSTQ_POS(15) BSTQ_POS(14)
-            BSTQ_POS(13) BSTQ_POS(12) BSTQ_POS(11) BSTQ_POS(10) BSTQ_POS(9) BSTQ_POS(8)
-            BSTQ_POS(7) BSTQ_POS(6) BSTQ_POS(5) BSTQ_POS(4) BSTQ_POS(3) BSTQ_POS(2)
-            BSTQ_POS(1)
+    }
+        BSTQ_GROUPED_SWITCH(KEXIT, group_case<NM>(top), BSTQ_POS)
 #undef BSTQ_POS
-        default:
-            break;
-        }
         last = 0;
     pass_done:
         Q.end(last, (m_touch >> last) & 1u);

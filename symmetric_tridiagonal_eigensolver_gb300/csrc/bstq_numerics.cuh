@@ -132,42 +132,34 @@ __device__ __forceinline__ T hyp1(T x)
 
 // ---------------------------------------------------------------------------
 // lartg: G(c,s) = [[c,-s],[s,c]] with G^T [f; g] = [r; 0], r = hypot(f, g);
-// g == 0 returns (1, 0, f) through a final select.
+// g == 0 returns (1, 0, f) through a final select (page "perf_steqr":
+// identity rotations must not diverge).
 //
-// float: r2 = f^2 + g^2 and y = rsqrt(r2) give c = f y, s = g y, r = r2 y
-// while r2 is a comfortably normal number; otherwise (a rare, divergent
-// branch) f and g are first multiplied by the power of two 2^-k that brings
-// max(|f|, |g|) into [1, 2), so the sum of squares can neither overflow nor
-// underflow, and r is scaled back by 2^k (page "perf_steqr": in-range fast
-// path, scaled path for the rest).
-// double: always the scaled form; the exponent arithmetic runs on the
-// integer pipe, which is idle next to the FP64 pipe.
+// float: branch free.  f and g are multiplied by the power of two 2^-k that
+// brings max(|f|, |g|) into [1, 2) (k read from the exponent field on the
+// integer pipe), so the sum of squares can neither overflow nor underflow;
+// c and s follow from one reciprocal square root, and r = f c + g s (which
+// equals (f^2 + g^2) / r) needs no scale-back.  A guarded fast path with a
+// rare scaled branch measured slower here: the branch splits the unrolled
+// chase into one basic block per position, so the eigenvector update of one
+// position can no longer overlap the dependency chain of the next.
+// double: the exponent arithmetic likewise runs on the integer pipe, which
+// is idle next to the FP64 pipe.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void lartg_scaled(float f, float g, float &c, float &s, float &r)
+__device__ __forceinline__ void lartg(float f, float g, float &c, float &s, float &r)
 {
     const unsigned fb = __float_as_uint(f) & 0x7fffffffu;
     const unsigned gb = __float_as_uint(g) & 0x7fffffffu;
-    int ew = (int)(max(fb, gb) >> 23);
-    ew = min(max(ew, 1), 253);
-    const float sc = __uint_as_float((unsigned)(254 - ew) << 23);  // 2^(127-ew)
-    const float isc = __uint_as_float((unsigned)ew << 23);         // 2^(ew-127)
+    // exponent field of max(|f|, |g|) in place, clamped to [1, 253]
+    unsigned eb = max(fb, gb) & 0x7f800000u;
+    eb = min(max(eb, 0x00800000u), 0x7e800000u);
+    const float sc = __uint_as_float(0x7f000000u - eb);  // 2^(127 - exponent)
     const float fs = f * sc, gs = g * sc;
     const float r2 = fmaf(fs, fs, gs * gs);
     const float y = rsqrt_nr(r2);
     c = fs * y;
     s = gs * y;
-    r = (r2 * y) * isc;
-}
-
-__device__ __forceinline__ void lartg(float f, float g, float &c, float &s, float &r)
-{
-    const float r2 = fmaf(f, f, g * g);
-    const float y = rsqrt_nr(r2);
-    c = f * y;
-    s = g * y;
-    r = r2 * y;
-    if (!(r2 >= 0x1p-100f && r2 <= 0x1p100f))
-        lartg_scaled(f, g, c, s, r);
+    r = fmaf(f, c, g * s);
     const bool z = g == 0.0f;
     c = z ? 1.0f : c;
     s = z ? 0.0f : s;

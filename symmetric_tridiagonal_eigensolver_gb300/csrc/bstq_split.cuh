@@ -71,31 +71,21 @@ struct QApplier {
     // the sign of a zero), so every streamed column is written back
     __device__ __forceinline__ void pass(int rhi, int rlo)
     {
-        Q.begin(rhi);
+        const int top = group_top<NM, KEXIT>(rhi);
+        Q.begin(top);
         int last = 0;
-        switch (rhi) {
 #define BSTQ_APOS(C)                                                         \
-    case C:                                                                  \
-        if constexpr (C <= NM - 1) {                                         \
-            apply_at<C>();                                                   \
-            if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                 \
-                if (C - 1 < rlo) {                                           \
-                    last = C - 1;                                            \
-                    goto applied;                                            \
-                }                                                            \
+    if constexpr (C <= NM - 1) {                                             \
+        apply_at<C>();                                                       \
+        if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                     \
+            if (C - 1 < rlo) {                                               \
+                last = C - 1;                                                \
+                goto applied;                                                \
             }                                                                \
         }                                                                    \
-        [[fallthrough]];
-            BSTQ_APOS(31) BSTQ_APOS(30) BSTQ_APOS(29) BSTQ_APOS(28) BSTQ_APOS(27) BSTQ_APOS(26)
-            BSTQ_APOS(25) BSTQ_APOS(24) BSTQ_APOS(23) BSTQ_APOS(22) BSTQ_APOS(21) BSTQ_APOS(20)
-            BSTQ_APOS(19) BSTQ_APOS(18) BSTQ_APOS(17) BSTQ_APOS(16) BSTQ_APOS(15) BSTQ_APOS(14)
-            BSTQ_APOS(13) BSTQ_APOS(12) BSTQ_APOS(11) BSTQ_APOS(10) BSTQ_APOS(9) BSTQ_APOS(8)
-            BSTQ_APOS(7) BSTQ_APOS(6) BSTQ_APOS(5) BSTQ_APOS(4) BSTQ_APOS(3) BSTQ_APOS(2)
-            BSTQ_APOS(1)
+    }
+        BSTQ_GROUPED_SWITCH(KEXIT, group_case<NM>(top), BSTQ_APOS)
 #undef BSTQ_APOS
-        default:
-            break;
-        }
         last = 0;
     applied:
         Q.end(last, true);
