@@ -189,7 +189,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         // 32 * kSplitPairs problems per block; shared memory as SplitSmem<nm>
         const int P = kSplitPairs;
         const int rr = nm <= 12 ? nm : 12;
-        size_t off = 2ull * nm * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
+        size_t off = (2ull * nm + 1) * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
                      size_t(P) * 32 * (16 + nm);
         off = (off + 15) / 16 * 16;
         pl.smem = off + size_t(P) * 32 * nm * (nm - rr) * 4;
@@ -207,13 +207,18 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     }
     const size_t elem = dtype ? 8 : 4;
     const size_t mem_per_thread = jobz ? size_t(nm) * memory_rows(dtype, nm, qs) * elem : 0;
-    // shared memory per thread: the memory rows of Q (shared / hybrid) and
-    // the mirror of d and e the settle step reads at dynamic positions
-    const size_t smem_per_thread =
-        ((family == FAMILY_STATIC && (qs == QS_SMEM || qs == QS_HYBRID)) ? mem_per_thread : 0) +
-        2 * size_t(nm) * elem +
-        // column scales of the factored double eigenvector update
-        ((family == FAMILY_DYNAMIC && dtype == BSTQ_F64 && jobz) ? 2 * size_t(nm) * elem : 0);
+    size_t smem_per_thread;
+    if (family == FAMILY_STATIC) {
+        // the shared rows of Q (shared / hybrid), then the lane-major mirror
+        // of d and e the settle step reads at dynamic positions, 2 nm + 1
+        // elements per lane
+        smem_per_thread = ((qs == QS_SMEM || qs == QS_HYBRID) && jobz ? mem_per_thread : 0) +
+                          (2 * size_t(nm) + 1) * elem;
+    } else {
+        // d and e in shared memory, plus the column scales of the factored
+        // double eigenvector update
+        smem_per_thread = 2 * size_t(nm) * elem + ((dtype == BSTQ_F64 && jobz) ? 2 * size_t(nm) * elem : 0);
+    }
     // Threads an SM can hold for this kernel.
     const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
     int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);

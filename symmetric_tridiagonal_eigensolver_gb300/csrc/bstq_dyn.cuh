@@ -238,83 +238,89 @@ struct DynLane {
         inblock = false;
     }
 
-    // One settle event; true while the lane still needs settling.
-    __device__ bool settle_step()
+    // Settle the lane (advance past converged eigenvalues and blocks until
+    // it has a task, is done or has exhausted its budget); consecutive
+    // deflations are handled in one call.
+    __device__ void settle_step()
     {
-        if (!inblock) {
-            if (bnext >= n) {
-                status = ST_DONE;
-                return false;
+        int mm;
+        for (;;) {
+            if (!inblock) {
+                if (bnext >= n) {
+                    status = ST_DONE;
+                    return;
+                }
+                lb = bnext;
+                le = block_hi(zmask, lb);
+                bnext = le + 1;
+                if (le == lb)
+                    continue;
+                anorm = block_norm(lb, le);
+                if (anorm == T(0))
+                    continue;
+                scale_factors(anorm, iscale, pre, sc, aeff);
+                if (iscale)
+                    scale_range(pre, sc, true);
+                lo = lb;
+                inblock = true;
             }
-            lb = bnext;
-            le = block_hi(zmask, lb);
-            bnext = le + 1;
-            if (le == lb)
-                return true;
-            anorm = block_norm(lb, le);
-            if (anorm == T(0))
-                return true;
-            scale_factors(anorm, iscale, pre, sc, aeff);
-            if (iscale)
-                scale_range(pre, sc, true);
-            lo = lb;
-            inblock = true;
-        }
-        // first negligible off-diagonal from lo (page "algo_steqr")
-        int mm = le;
-        T dcur = D(lo);
-        for (int i = lo; i < le; ++i) {
-            const T dn = D(i + 1);
-            const T ev = Ev(i);
-            bool neg;
-            if constexpr (sizeof(T) == 8) {
-                // Exponent bounds first (integer pipe).  With k the biased
-                // exponent field, 2^(k-1023) <= |x| < 2^(k-1022) (the upper
-                // bound holds for zero and subnormals too), so
-                // e^2 >= 2^(2 k_e - 2046), eps^2 |d_i d_i+1| < 2^(k_1 + k_2 - 2150)
-                // and safmin = 2^-1022.  When 2 k_e >= k_1 + k_2 - 99 and
-                // 2 k_e >= 1037, e^2 exceeds each term of the threshold by a
-                // factor of 8 or more, so the off-diagonal is certainly not
-                // negligible and the FP64 test is skipped.  (Scaled inputs
-                // are finite here.)
-                const int ke = (__double2hiint(ev) >> 20) & 0x7ff;
-                const int k1 = (__double2hiint(dcur) >> 20) & 0x7ff;
-                const int k2 = (__double2hiint(dn) >> 20) & 0x7ff;
-                const bool clear = (2 * ke > k1 + k2 - 100) && (2 * ke > 1036);
-                neg = false;
-                if (!clear) {
+            // first negligible off-diagonal from lo (page "algo_steqr")
+            mm = le;
+            T dcur = D(lo);
+            for (int i = lo; i < le; ++i) {
+                const T dn = D(i + 1);
+                const T ev = Ev(i);
+                bool neg;
+                if constexpr (sizeof(T) == 8) {
+                    // Exponent bounds first (integer pipe).  With k the biased
+                    // exponent field, 2^(k-1023) <= |x| < 2^(k-1022) (the upper
+                    // bound holds for zero and subnormals too), so
+                    // e^2 >= 2^(2 k_e - 2046), eps^2 |d_i d_i+1| < 2^(k_1 + k_2 - 2150)
+                    // and safmin = 2^-1022.  When 2 k_e >= k_1 + k_2 - 99 and
+                    // 2 k_e >= 1037, e^2 exceeds each term of the threshold by a
+                    // factor of 8 or more, so the off-diagonal is certainly not
+                    // negligible and the FP64 test is skipped.  (Scaled inputs
+                    // are finite here.)
+                    const int ke = (__double2hiint(ev) >> 20) & 0x7ff;
+                    const int k1 = (__double2hiint(dcur) >> 20) & 0x7ff;
+                    const int k2 = (__double2hiint(dn) >> 20) & 0x7ff;
+                    const bool clear = (2 * ke > k1 + k2 - 100) && (2 * ke > 1036);
+                    neg = false;
+                    if (!clear) {
+                        const T ae = dabs(ev);
+                        const T tst = ae * ae;
+                        const T thr = fma(C_::eps2 * dabs(dcur), dabs(dn), C_::safmin);
+                        // non-negative doubles order as their bit patterns
+                        neg = __double_as_longlong(tst) <= __double_as_longlong(thr);
+                    }
+                } else {
                     const T ae = dabs(ev);
                     const T tst = ae * ae;
                     const T thr = fma(C_::eps2 * dabs(dcur), dabs(dn), C_::safmin);
-                    // non-negative doubles order as their bit patterns
-                    neg = __double_as_longlong(tst) <= __double_as_longlong(thr);
+                    neg = tst <= thr;
                 }
-            } else {
-                const T ae = dabs(ev);
-                const T tst = ae * ae;
-                const T thr = fma(C_::eps2 * dabs(dcur), dabs(dn), C_::safmin);
-                neg = tst <= thr;
+                if (neg) {
+                    mm = i;
+                    break;
+                }
+                dcur = dn;
             }
-            if (neg) {
-                mm = i;
+            if (mm < le)
+                setE(mm, T(0));
+            if (mm != lo)
                 break;
-            }
-            dcur = dn;
-        }
-        if (mm < le)
-            setE(mm, T(0));
-        if (mm == lo) {
-            ++lo;
+            ++lo;  // eigenvalue at lo has converged
             if (lo > le)
                 close_block();
-            return true;
         }
         const T d1 = D(lo), d2 = D(lo + 1), e1 = Ev(lo);
-        if (mm == lo + 1) {
-            solve2x2(d1, e1, d2, cs2, sn2);
+        T t, mu;
+        shift_tangent(d1, d2, e1, t, mu);
+        if (mm == lo + 1) {  // 2x2 direct solve
+            rot_from_tangent(t, cs2, sn2);
             task = TASK_2X2;
             m = lo + 1;
-            return false;
+            return;
         }
         if (jtot == budget) {
             unscale_block(true);
@@ -323,15 +329,13 @@ struct DynLane {
                 cnt += Ev(i) != T(0) ? 1 : 0;
             info = cnt;
             status = ST_FAIL;
-            return false;
+            return;
         }
         ++jtot;
-        const T mu = wilkinson_shift(d1, d2, e1);
         f = D(mm) - mu;
         g = Ev(mm - 1);
         m = mm;
         task = TASK_SWEEP;
-        return false;
     }
 
     __device__ __forceinline__ bool has_task() const { return status == ST_RUN && task != TASK_NONE; }
@@ -499,11 +503,9 @@ __global__ void dyn_kernel(KParams p)
 
     if (SCHED == SCHED_FLAT) {
         for (;;) {
-            bool need = (L.status == ST_RUN) && (L.task == TASK_NONE);
-            while (__any_sync(FULL, need)) {
-                if (need)
-                    need = L.settle_step();
-            }
+            // settle every lane without a task (one call settles it fully)
+            if (L.status == ST_RUN && L.task == TASK_NONE)
+                L.settle_step();
             const bool has = L.has_task();
             if (!__any_sync(FULL, has))
                 break;

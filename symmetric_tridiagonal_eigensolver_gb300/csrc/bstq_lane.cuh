@@ -108,8 +108,10 @@ struct El<double> {
 // streaming rotation apply).  Memory layout in 16-byte vectors, vector g of
 // column k of thread t at base[(k*G + g)*stride + t]: the lanes of a warp
 // touch consecutive vectors whatever column they are on, so shared memory is
-// accessed without bank conflicts.  Loads are unconditional (every lane's
-// region holds finite values); stores only write columns a lane changed.
+// accessed without bank conflicts and global memory is coalesced.  (A
+// lane-major layout with an odd lane pitch, whose addresses are compile-time
+// offsets, measured slower for the hybrid store.)  Loads are unconditional
+// (every lane's region holds finite values).
 template <typename T, int NM, int RR, int MR>
 struct QMix {
     using Tr = El<T>;
@@ -128,16 +130,20 @@ struct QMix {
     V16 *base;
     int stride;
 
+    // bytes of the memory rows per thread
+    static constexpr int MEM_BYTES = NM * G * 16;
+
     __device__ __forceinline__ void setup(void *p, int s)
     {
         base = reinterpret_cast<V16 *>(p);
         stride = s;
     }
+    __device__ __forceinline__ int vidx(int k, int g) const { return (k * G + g) * stride; }
     __device__ __forceinline__ void load(int k, E (&x)[NEM > 0 ? NEM : 1]) const
     {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const V16 v = base[(k * G + g) * stride];
+            const V16 v = base[vidx(k, g)];
             x[2 * g] = v.a;
             x[2 * g + 1] = v.b;
         }
@@ -146,7 +152,7 @@ struct QMix {
     {
 #pragma unroll
         for (int g = 0; g < G; ++g)
-            base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
+            base[vidx(k, g)] = V16{x[2 * g], x[2 * g + 1]};
     }
     __device__ __forceinline__ void init_col(int s, int row_of_one)
     {
@@ -222,6 +228,7 @@ struct QMix {
 // Empty store for eigenvalues only.
 template <typename T, int NM>
 struct QNone {
+    static constexpr int MEM_BYTES = 0;
     __device__ __forceinline__ void setup(void *, int) {}
     __device__ __forceinline__ void init_col(int, int) {}
     __device__ __forceinline__ void begin(int) {}
@@ -389,8 +396,8 @@ struct Lane {
     int n, status, info;
     unsigned zmask;    // block boundaries (input exact zeros, i >= n-1)
     unsigned revmask;  // bit lb: block starting at lb was mirrored
-    unsigned dmask;    // deflation test results over [lo, le)
-    bool dvalid, inblock;
+    unsigned tmask;    // deflation test result of every e_i, for the current values
+    bool inblock;
     int bnext, lb, le, lo;
     int iscale;
     T pre, sc, aeff, anorm;
@@ -405,10 +412,11 @@ struct Lane {
     // rotation, first rotation, "e_C <- r", columns this lane changes
     int hi_l, lo_l;
     unsigned m_in, m_act, m_22, m_first, m_er, m_touch;
-    // shared-memory mirror of d and e for the settle step's dynamic reads:
-    // entry i of d at mir[i * mstride], of e at mir[(NM + i) * mstride]
+    // shared-memory mirror of d and e for the settle step's dynamic reads,
+    // lane-major: entry i of d at mir[i], of e at mir[NM + i]; lanes are
+    // MIRROR_PITCH = 2 NM + 1 elements apart (odd: no bank conflicts)
+    static constexpr int MIRROR_PITCH = 2 * NM + 1;
     T *mir;
-    int mstride;
 
     // Storage index s -> caller's index.
     __device__ __forceinline__ int phys(int s) const
@@ -460,7 +468,7 @@ struct Lane {
         jtot = 0;
         task = TASK_NONE;
         inblock = false;
-        dvalid = false;
+        tmask = 0;
         bnext = 0;
         lb = le = lo = m = 0;
         info = 0;
@@ -569,82 +577,115 @@ struct Lane {
     }
 
     // Relative deflation test (page "algo_steqr"):
-    // |e_i|^2 <= eps^2 |d_i| |d_{i+1}| + safmin, for i in [lo, le).  An
-    // off-diagonal found negligible earlier counts as the exact zero it was
-    // set to (it is never read as a coupling again).
-    __device__ __forceinline__ unsigned deflation_mask() const
+    // |e_i|^2 <= eps^2 |d_i| |d_{i+1}| + safmin.
+    __device__ __forceinline__ static bool negligible(T ei, T di, T dn)
+    {
+        const T ae = dabs(ei);
+        const T tst = ae * ae;
+        const T thr = fma(C_::eps2 * dabs(di), dabs(dn), C_::safmin);
+        if constexpr (sizeof(T) == 8)  // non-negative doubles order as their bits
+            return __double_as_longlong(tst) <= __double_as_longlong(thr);
+        else
+            return tst <= thr;
+    }
+
+    // Entry i's values are final for this pass: copy d_i and e_i to the
+    // mirror and record the deflation test of e_i.  The chase calls this for
+    // each position once that position's values are final, and for the two
+    // entries below the last position when the pass ends, so the settle step
+    // finds the mirror and the test bits of every entry current without
+    // recomputing them.
+    template <int I>
+    __device__ __forceinline__ void settle_entry()
+    {
+        if constexpr (I >= 0 && I <= NM - 1) {
+            mir[I] = d[I];
+            mir[NM + I] = e[I];
+            if constexpr (I <= NM - 2) {
+                const bool ng = negligible(e[I], d[I], d[I + 1]);
+                tmask = ng ? (tmask | (1u << I)) : (tmask & ~(1u << I));
+            }
+        }
+    }
+
+    // Every entry (after loading or scaling a block, and after a nested pass).
+    __device__ __forceinline__ void refresh_all()
     {
         unsigned mk = 0;
 #pragma unroll
-        for (int i = 0; i < NM - 1; ++i) {
-            const T ae = dabs(e[i]);
-            const T tst = ae * ae;
-            const T thr = fma(C_::eps2 * dabs(d[i]), dabs(d[i + 1]), C_::safmin);
-            mk |= (tst <= thr) ? (1u << i) : 0u;
-        }
-        const unsigned range = ((1u << le) - 1u) & (~0u << lo);
-        return (mk | zeroed) & range;
-    }
-
-    __device__ __forceinline__ void write_mirror() const
-    {
-#pragma unroll
         for (int i = 0; i < NM; ++i) {
-            mir[i * mstride] = d[i];
-            mir[(NM + i) * mstride] = e[i];
+            mir[i] = d[i];
+            mir[NM + i] = e[i];
         }
+#pragma unroll
+        for (int i = 0; i < NM - 1; ++i)
+            mk |= negligible(e[i], d[i], d[i + 1]) ? (1u << i) : 0u;
+        tmask = mk;
     }
-    __device__ __forceinline__ T mir_d(int i) const { return mir[i * mstride]; }
-    __device__ __forceinline__ T mir_e(int i) const { return mir[(NM + i) * mstride]; }
 
-    // One settle event.  Returns true while the lane has no chase task and is
-    // still running.
-    __device__ bool settle_step()
+    __device__ __forceinline__ T mir_d(int i) const { return mir[i]; }
+    __device__ __forceinline__ T mir_e(int i) const { return mir[NM + i]; }
+
+    // Settle the lane: advance past converged eigenvalues and blocks until
+    // the lane has a task (2x2 solve or sweep), is done, or has exhausted
+    // its sweep budget.  Consecutive deflations are handled in one call, so
+    // a lockstep warp computes the shifts of all its lanes together.
+    __device__ void settle_step()
     {
-        if (!inblock) {
-            if (bnext >= n) {
-                status = ST_DONE;
-                return false;
+        int mm;
+        for (;;) {
+            if (!inblock) {
+                if (bnext >= n) {
+                    status = ST_DONE;
+                    return;
+                }
+                lb = bnext;
+                le = block_hi(zmask, lb);
+                bnext = le + 1;
+                if (le == lb)
+                    continue;  // 1x1 block: final
+                anorm = block_norm(lb, le);
+                if (anorm == T(0))
+                    continue;  // zero block: final
+                scale_factors(anorm, iscale, pre, sc, aeff);
+                if (iscale)
+                    scale_block(pre, sc);
+                lo = lb;
+                inblock = true;
+                refresh_all();
             }
-            lb = bnext;
-            le = block_hi(zmask, lb);
-            bnext = le + 1;
-            if (le == lb)
-                return true;  // 1x1 block: final
-            anorm = block_norm(lb, le);
-            if (anorm == T(0))
-                return true;  // zero block: final
-            scale_factors(anorm, iscale, pre, sc, aeff);
-            if (iscale)
-                scale_block(pre, sc);
-            lo = lb;
-            inblock = true;
-            dvalid = false;
-        }
-        if (!dvalid) {
-            write_mirror();
-            dmask = deflation_mask();
-            dvalid = true;
-        }
-        const int mm = __ffs(dmask | (1u << le)) - 1;
-        if (mm < le)
-            zeroed |= 1u << mm;  // e_mm <- 0
-        if (mm == lo) {  // eigenvalue at lo has converged
-            ++lo;
-            if (lo > le)
+            // negligible off-diagonals of the active range [lo, le); one
+            // found negligible earlier counts as the exact zero it was set to
+            unsigned dmask = (tmask | zeroed) & ((1u << le) - 1u) & (~0u << lo);
+            // Eigenvalues lo, lo+1, ... have converged while e_lo, e_lo+1,
+            // ... are negligible: skip that run of set bits in one step (bit
+            // le stands for the block end; a run through it closes the
+            // block).  Every negligible e_i passed over, and the first one
+            // after the run, is set to zero.
+            const unsigned long long x = (unsigned long long)(dmask | (1u << le)) >> lo;
+            const int run = __ffsll((long long)~x) - 1;
+            const unsigned below_le = (1u << le) - 1u;
+            zeroed |= (unsigned)((((1ull << run) - 1ull) << lo)) & below_le;
+            lo += run;
+            if (lo > le) {
                 close_block();
-            else
-                dmask &= ~0u << lo;
-            return true;
+                continue;
+            }
+            dmask &= ~0u << lo;
+            mm = __ffs(dmask | (1u << le)) - 1;  // > lo
+            if (mm < le)
+                zeroed |= 1u << mm;  // e_mm <- 0
+            break;
         }
+        // Shift and 2x2 rotation from one evaluation, without branches: the
+        // lanes of a warp settling together need not split by task.
         const T d1 = mir_d(lo), d2 = mir_d(lo + 1), e1 = mir_e(lo);
-        if (mm == lo + 1) {  // 2x2 direct solve, applied in the next pass
-            solve2x2(d1, e1, d2, cs2, sn2);
-            task = TASK_2X2;
-            m = lo + 1;
-            return false;
-        }
-        if (jtot == budget) {  // sweep budget exhausted
+        const T dm = mir_d(mm), gm = mir_e(mm - 1);
+        T t, mu;
+        shift_tangent(d1, d2, e1, t, mu);
+        rot_from_tangent(t, cs2, sn2);  // used by a 2x2 solve only
+        const bool two = mm == lo + 1;  // 2x2 direct solve, applied in the next pass
+        if (!two && jtot == budget) {  // sweep budget exhausted
             unscale_block(true);
             int cnt = 0;
 #pragma unroll
@@ -653,15 +694,13 @@ struct Lane {
                     ++cnt;
             info = cnt;
             status = ST_FAIL;
-            return false;
+            return;
         }
-        ++jtot;
-        const T mu = wilkinson_shift(d1, d2, e1);
-        f0 = mir_d(mm) - mu;
-        g0 = mir_e(mm - 1);
+        jtot += two ? 0 : 1;
+        f0 = dm - mu;
+        g0 = gm;
         m = mm;
-        task = TASK_SWEEP;
-        return false;
+        task = two ? TASK_2X2 : TASK_SWEEP;
     }
 
     __device__ __forceinline__ bool has_task() const { return status == ST_RUN && task != TASK_NONE; }
@@ -738,6 +777,7 @@ struct Lane {
             e[C - 2] = cs * eo;
         }
         f = en;
+        settle_entry<C>();
         Q.template rot<C>(cs, sn, (m_touch >> C) & 1u);
     }
 
@@ -756,6 +796,8 @@ struct Lane {
         if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                     \
             if (C - 1 < rlo) {                                               \
                 last = C - 1;                                                \
+                settle_entry<C - 1>();                                       \
+                settle_entry<C - 2>();                                       \
                 goto pass_done;                                              \
             }                                                                \
         }                                                                    \
@@ -763,6 +805,7 @@ struct Lane {
         BSTQ_GROUPED_SWITCH(KEXIT, group_case<NM>(top), BSTQ_POS)
 #undef BSTQ_POS
         last = 0;
+        settle_entry<0>();
     pass_done:
         Q.end(last, (m_touch >> last) & 1u);
     }
@@ -783,6 +826,7 @@ struct Lane {
         Q.begin(hi_l);
         own_positions<NM - 1>(Q);
         Q.end(lo_l - 1, true);
+        refresh_all();
     }
 
     __device__ __forceinline__ void post_pass()
@@ -794,7 +838,6 @@ struct Lane {
                 close_block();
         }
         task = TASK_NONE;
-        dvalid = false;
         clear_pass();
     }
 };
@@ -824,11 +867,12 @@ __global__ void lane_kernel(KParams p)
 
     // dynamic shared memory: [memory rows of Q (shared / hybrid)] [mirror]
     constexpr bool kQShared = WANTZ && (QS == QS_SMEM || QS == QS_HYBRID);
-    constexpr size_t kQBytesPerLane = kQShared ? size_t(NM) * QLayout<T, NM, QS>::MR * sizeof(T) : 0;
-    Lane<T, NM, KEXIT> L;
+    // (sizes as static_smem_per_thread() on the host side)
+    constexpr size_t kQBytesPerLane = kQShared ? size_t(QT::MEM_BYTES) : 0;
+    using LaneT = Lane<T, NM, KEXIT>;
+    LaneT L;
     L.mir = reinterpret_cast<T *>(reinterpret_cast<char *>(smem_raw) + kQBytesPerLane * blockDim.x) +
-            threadIdx.x;
-    L.mstride = blockDim.x;
+            threadIdx.x * LaneT::MIRROR_PITCH;
     L.load(p, b, live);
     QT Q;
     if constexpr (WANTZ) {
@@ -849,11 +893,9 @@ __global__ void lane_kernel(KParams p)
 
     if (SCHED == SCHED_FLAT) {
         for (;;) {
-            bool need = (L.status == ST_RUN) && (L.task == TASK_NONE);
-            while (__any_sync(FULL, need)) {
-                if (need)
-                    need = L.settle_step();
-            }
+            // settle every lane without a task (one call settles it fully)
+            if (L.status == ST_RUN && L.task == TASK_NONE)
+                L.settle_step();
             const bool has = L.has_task();
             if (!__any_sync(FULL, has))
                 break;

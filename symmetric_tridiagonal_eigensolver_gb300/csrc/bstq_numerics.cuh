@@ -1,6 +1,6 @@
 // Device building blocks of the steqr iteration: machine constants, Newton-
-// Raphson reciprocal / square-root kernels, lartg, the copysign shift and the
-// 2x2 direct solve.
+// Raphson reciprocal / square-root kernels, lartg, and the copysign shift
+// together with the 2x2 direct solve.
 //
 // Sources: BatchLAS page "algo_steqr" (deflation criterion, scaling, shift,
 // Givens rotation, EXP update, 2x2 solve) and BatchLAS page "perf_steqr",
@@ -107,7 +107,7 @@ __device__ __forceinline__ T div_nr(T a, T b)
     return fma(r, y, q);
 }
 
-// sqrt(x) for x >= 1 (the only use): s = x rsqrt(x) with one correction
+// sqrt(x) for a normal, finite x > 0: s = x rsqrt(x) with one correction
 // s + (x - s^2) / (2 s).
 template <typename T>
 __device__ __forceinline__ T sqrt_nr(T x)
@@ -146,13 +146,13 @@ __device__ __forceinline__ T hyp1(T x)
 // double: the exponent arithmetic likewise runs on the integer pipe, which
 // is idle next to the FP64 pipe.
 // ---------------------------------------------------------------------------
+// Requires max(|f|, |g|) < 2^126 (entries of a scaled block are below
+// 2^65).
 __device__ __forceinline__ void lartg(float f, float g, float &c, float &s, float &r)
 {
-    const unsigned fb = __float_as_uint(f) & 0x7fffffffu;
-    const unsigned gb = __float_as_uint(g) & 0x7fffffffu;
-    // exponent field of max(|f|, |g|) in place, clamped to [1, 253]
-    unsigned eb = max(fb, gb) & 0x7f800000u;
-    eb = min(max(eb, 0x00800000u), 0x7e800000u);
+    // exponent field of max(|f|, |g|, 2^-126) in place
+    const float mx = fmaxf(fmaxf(fabsf(f), fabsf(g)), 0x1p-126f);
+    const unsigned eb = __float_as_uint(mx) & 0x7f800000u;
     const float sc = __uint_as_float(0x7f000000u - eb);  // 2^(127 - exponent)
     const float fs = f * sc, gs = g * sc;
     const float r2 = fmaf(fs, fs, gs * gs);
@@ -212,31 +212,45 @@ __device__ __forceinline__ void lartg_scaled(double f, double g, double &c, doub
     r = z ? f : r;
 }
 
-// Copysign shift from the 2x2 block (d1, e1; e1, d2) at the converging end:
-// g = (d2 - d1) / (2 e1), r = sqrt(g^2 + 1), mu = d1 - e1 / (g + copysign(r, g)).
+// The leading 2x2 block (d1, e1; e1, d2) of the active block (e1 != 0, not
+// negligible) gives both the copysign shift of a sweep and the rotation of a
+// direct 2x2 solve (page "algo_steqr"):
+//   shift:  g = (d2 - d1) / (2 e1), r = sqrt(g^2 + 1),
+//           mu = d1 - e1 / (g + copysign(r, g));
+//   solve:  tau = (d2 - d1) / (2 e1) = g, t = the smaller root of
+//           t^2 + 2 tau t - 1 = 0, i.e. t = sgn(tau) / (|tau| + sqrt(tau^2 + 1));
+//           the rotation with tangent t diagonalises the block (eigenvalues
+//           d1 - t e1 and d2 + t e1).
+// Both follow from delta = (d2 - d1) / 2, h = sqrt(delta^2 + e1^2) and
+// q = 1 / (|delta| + h):
+//   t = sgn(tau) |e1| q,   mu = d1 - e1 t = d1 - sgn(delta) e1^2 q,
+// i.e. the shift is the eigenvalue of the 2x2 block nearer to d1 (multiply
+// the fractions above by |e1| / |e1|).  At delta = 0 exactly, sgn(tau) is
+// taken as sgn(e1) (tau = 0 / e1 carries e1's sign), so mu = d1 - |e1| as the
+// copysign form gives; t = +-1 both diagonalise the block.  One square root
+// and one reciprocal instead of the four of the two formulas evaluated
+// separately.  e1^2 > safmin in a scaled block, so delta^2 + e1^2 is a
+// normal number that does not overflow.
 template <typename T>
-__device__ __forceinline__ T wilkinson_shift(T d1, T d2, T e1)
+__device__ __forceinline__ void shift_tangent(T d1, T d2, T e1, T &t, T &mu)
 {
-    T g = div_nr(d2 - d1, T(2) * e1);
-    T r = hyp1(g);
-    return d1 - div_nr(e1, g + copysign(r, g));
+    const T dl = T(0.5) * (d2 - d1);
+    const T ae = dabs(e1);
+    const T h = sqrt_nr(fma(dl, dl, ae * ae));
+    const T q = rcp_nr(dabs(dl) + h);
+    const T at = ae * q;
+    t = ((dl < T(0)) != (e1 < T(0))) ? -at : at;
+    mu = fma(-e1, t, d1);
 }
 
-// Direct solve of the 2x2 block [[a, b], [b, c2]] (b != 0): the rotation
-// with tangent t, the smaller root of t^2 + 2 tau t - 1 = 0,
-// tau = (c2 - a) / (2 b), diagonalises it (eigenvalues a - t b and
-// c2 + t b).  Returns (cs, sn) of that rotation in the chase's column
-// convention for the pair (k + 1, k) with k the block's first index:
+// (cs, sn) of the 2x2 solve from its tangent t (|t| <= 1), in the chase's
+// column convention for the pair (k + 1, k), k the block's first index:
 //   q_{k+1} <- cs q_{k+1} + sn q_k,  q_k <- -sn q_{k+1} + cs q_k.
 template <typename T>
-__device__ __forceinline__ void solve2x2(T a, T b, T c2, T &cs, T &sn)
+__device__ __forceinline__ void rot_from_tangent(T t, T &cs, T &sn)
 {
-    T tau = div_nr(c2 - a, T(2) * b);
-    T sgn = tau < T(0) ? T(-1) : T(1);
-    T t = div_nr(sgn, dabs(tau) + hyp1(tau));
-    T cq = rcp_nr(hyp1(t));
-    cs = cq;
-    sn = t * cq;
+    cs = rsqrt_nr(fma(t, t, T(1)));
+    sn = t * cs;
 }
 
 // ---------------------------------------------------------------------------

@@ -93,14 +93,14 @@ struct QApplier {
 };
 
 // Shared-memory layout of one block (P pairs, 32 lanes each):
-//   mirror   : 2 * NM floats per chase lane             (Lane::mir)
+//   mirror   : 2 * NM + 1 floats per chase lane         (Lane::mir)
 //   rot      : [pair][parity][NM][32] float2             (recorded passes)
 //   ctrl     : [pair][parity] int2 (rhi, rlo); rhi < 0 ends the loop
 //   handoff  : per chase lane: zmask, revmask, status, n and pos[NM] bytes
 template <int NM>
 struct SplitSmem {
     static constexpr int P = kSplitPairs;
-    static constexpr size_t mirror = 2ull * NM * sizeof(float) * 32 * P;
+    static constexpr size_t mirror = (2ull * NM + 1) * sizeof(float) * 32 * P;
     static constexpr size_t rot = size_t(P) * 2 * NM * 32 * sizeof(float2);
     static constexpr size_t ctrl = size_t(P) * 2 * sizeof(int2);
     static constexpr size_t hand = size_t(P) * 32 * (4 * sizeof(int) + NM);
@@ -135,8 +135,7 @@ __global__ void __maxnreg__(128) split_kernel(KParams p)
 
     if (chase) {
         Lane<float, NM, KEXIT> L;
-        L.mir = reinterpret_cast<float *>(sm) + slot;
-        L.mstride = 32 * P;
+        L.mir = reinterpret_cast<float *>(sm) + slot * Lane<float, NM, KEXIT>::MIRROR_PITCH;
         L.load(p, b, live);
         hand[0 * 32 * P + slot] = (int)L.zmask;
         hand[1 * 32 * P + slot] = (int)L.revmask;
@@ -145,11 +144,9 @@ __global__ void __maxnreg__(128) split_kernel(KParams p)
         QRecorder<NM> Q;
         int parity = 0;
         for (;;) {
-            bool need = (L.status == ST_RUN) && (L.task == TASK_NONE);
-            while (__any_sync(FULL, need)) {
-                if (need)
-                    need = L.settle_step();
-            }
+            // settle every lane without a task (one call settles it fully)
+            if (L.status == ST_RUN && L.task == TASK_NONE)
+                L.settle_step();
             const bool has = L.has_task();
             const bool any = __any_sync(FULL, has);
             int rhi = -1, rlo = NM;
