@@ -45,11 +45,28 @@ COMPANIONS = [dict(dtype="float32", n=8, batch=65536, jobz=True),
 # (BatchLAS perf_steqr, "What ships" table: 450.9 us per call).
 PAGES_BASELINE = 32768 / 450.9e-6
 # DRAM bytes (read + write) per launch measured by ncu for a kernel variant,
-# keyed by bstq_describe()'s text; a changed kernel no longer matches and
-# reports null (profiles/lane_f32_n16_V_batch32768.md).
-NCU_TRAFFIC = {
-    "lane<f32,16,V,hybrid,flat> tpb=224 grid=147 smem=143360 regs=255 work=131072": 4.72e6,
-}
+# keyed by bstq_describe()'s text and the digest of the CUDA sources
+# (kernel_digest()); a changed kernel no longer matches and reports null
+# (profiles/lane_f32_n16_V_batch32768.md).
+NCU_TRAFFIC = {}
+
+
+def kernel_digest() -> str:
+    """Short SHA-256 over the library's CUDA sources (csrc/*.cu, *.cuh, *.h,
+    *.inc) and its header, in name order."""
+    import hashlib
+    pkg = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300")
+    files = sorted(os.path.join(pkg, "csrc", f) for f in os.listdir(os.path.join(pkg, "csrc"))
+                   if f.endswith((".cu", ".cuh", ".h", ".inc")))
+    files.append(os.path.join(ROOT, "include", "bstq.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 SM_FP32_LANES = 128     # FP32 FMA lanes per SM (Blackwell SM)
 SM_FP64_LANES = 2       # FP64 FMA lanes per SM on GB300 (1.25 TFLOP/s nominal)
 
@@ -364,6 +381,7 @@ def main():
             tdist.destroy_process_group()
         return 0
     counts = oracle_counts(HEADLINE, d, e)
+    digest = kernel_digest()
     flops, bytes_ = algorithmic(HEADLINE, counts)
     t = mean_ms / 1e3
     value = total_problems / t
@@ -376,9 +394,10 @@ def main():
         "config": {"workload": wl_name(HEADLINE), "per_gpu_batch": HEADLINE["batch"],
                    "parallelism": f"replicas x{world} (independent problems, no collective)",
                    "l2": "flushed between steps (256 MiB write)", "kernel": desc,
+                   "kernel_digest": digest,
                    "sweep_budget": "30 per eigenvalue"},
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": fp32_peak / 1e12,
-                     "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": NCU_TRAFFIC.get(desc),
+                     "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": NCU_TRAFFIC.get((desc, digest)),
                      "roofline_fraction": roof_t / t,
                      "peak_source": f"derived: {sms} SMs x {SM_FP32_LANES} FP32 lanes x 2 x {sm_max_mhz:.0f} MHz",
                      "algorithmic_gflop_per_launch": flops / 1e9, "algorithmic_mb_per_launch": bytes_ / 1e6,

@@ -159,14 +159,14 @@ int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
  * The call itself allocates nothing and calls no allocating routine.
  *   d, e, Q   as for bstq_solve (device memory); Q is required.
  *   info      device int32[batch], receives the per-problem status.
- *   p         optional parameters; p->qstore is ignored.
- * Sizes: n in 13..32 for float and 9..32 for double (smaller problems keep Q
- * in registers and need no scratch at all: call bstq_solve with a `work`
- * buffer of align256(4 * batch) bytes, which only receives info; for them
- * this call returns -10).
+ *   p         optional parameters; p->qstore is ignored.  With p->kernel
+ *             left at BSTQ_KERNEL_AUTO, sizes whose static-position kernel
+ *             keeps Q in registers (float n <= 12, double n <= 8) run the
+ *             dynamic-position kernel, which keeps Q in the scratch array;
+ *             p->kernel = BSTQ_KERNEL_STATIC for those sizes returns -10.
  * Returns 0; -2 when jobz is not BSTQ_JOBZ_V; -4 when the problems need more
  * scratch than the array holds (n_pad^2 * sizeof(element) bytes per problem
- * slot, n_pad = n rounded up to 12, 16, 24 or 32, slots = batch rounded up to
+ * slot, n_pad = n rounded up to 4, 8, 12, 16, 24 or 32, slots = batch rounded up to
  * the block size; e.g. about 58,000 double problems of n <= 12 fit, or 16,000
  * float problems of n <= 32); other codes as bstq_solve_ex.
  * The first call on each device looks up the array's device address (with

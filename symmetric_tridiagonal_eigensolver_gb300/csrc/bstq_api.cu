@@ -189,7 +189,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         // 32 * kSplitPairs problems per block; shared memory as SplitSmem<nm>
         const int P = kSplitPairs;
         const int rr = nm <= 12 ? nm : 12;
-        size_t off = (2ull * nm + 1) * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
+        size_t off = 2ull * nm * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
                      size_t(P) * 32 * (16 + nm);
         off = (off + 15) / 16 * 16;
         pl.smem = off + size_t(P) * 32 * nm * (nm - rr) * 4;
@@ -209,11 +209,11 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     const size_t mem_per_thread = jobz ? size_t(nm) * memory_rows(dtype, nm, qs) * elem : 0;
     size_t smem_per_thread;
     if (family == FAMILY_STATIC) {
-        // the shared rows of Q (shared / hybrid), then the lane-major mirror
-        // of d and e the settle step reads at dynamic positions, 2 nm + 1
-        // elements per lane
+        // the shared rows of Q (shared / hybrid), then the mirror of d and e
+        // the settle step reads at dynamic positions, 2 nm elements per lane
+        // (tpb is a multiple of 32: whole warps)
         smem_per_thread = ((qs == QS_SMEM || qs == QS_HYBRID) && jobz ? mem_per_thread : 0) +
-                          (2 * size_t(nm) + 1) * elem;
+                          2 * size_t(nm) * elem;
     } else {
         // d and e in shared memory, plus the column scales of the factored
         // double eigenvector update
@@ -536,6 +536,12 @@ extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64
     q.qstore = BSTQ_QSTORE_GLOBAL;
     Plan pl;
     rc = make_plan(dtype, jobz, n, batch, &q, pl);
+    if (rc == -10 && q.kernel == 0) {
+        // the static family keeps small Q in registers and has no scratch
+        // variant there; the dynamic family covers every n
+        q.kernel = BSTQ_KERNEL_DYNAMIC;
+        rc = make_plan(dtype, jobz, n, batch, &q, pl);
+    }
     if (rc)
         return rc;
     if (pl.k->qs != QS_GLOBAL)

@@ -413,9 +413,11 @@ struct Lane {
     int hi_l, lo_l;
     unsigned m_in, m_act, m_22, m_first, m_er, m_touch;
     // shared-memory mirror of d and e for the settle step's dynamic reads,
-    // lane-major: entry i of d at mir[i], of e at mir[NM + i]; lanes are
-    // MIRROR_PITCH = 2 NM + 1 elements apart (odd: no bank conflicts)
-    static constexpr int MIRROR_PITCH = 2 * NM + 1;
+    // per warp [entry][lane]: entry i of d at mir[i * 32], of e at
+    // mir[(NM + i) * 32], mir = warp region + lane.  Static entries are
+    // compile-time offsets from the lane's base, and dynamic reads hit one
+    // bank per lane whatever entry each lane reads.
+    static constexpr int MIRROR_WARP_ELEMS = 2 * NM * 32;
     T *mir;
 
     // Storage index s -> caller's index.
@@ -599,8 +601,8 @@ struct Lane {
     __device__ __forceinline__ void settle_entry()
     {
         if constexpr (I >= 0 && I <= NM - 1) {
-            mir[I] = d[I];
-            mir[NM + I] = e[I];
+            mir[I * 32] = d[I];
+            mir[(NM + I) * 32] = e[I];
             if constexpr (I <= NM - 2) {
                 const bool ng = negligible(e[I], d[I], d[I + 1]);
                 tmask = ng ? (tmask | (1u << I)) : (tmask & ~(1u << I));
@@ -614,8 +616,8 @@ struct Lane {
         unsigned mk = 0;
 #pragma unroll
         for (int i = 0; i < NM; ++i) {
-            mir[i] = d[i];
-            mir[NM + i] = e[i];
+            mir[i * 32] = d[i];
+            mir[(NM + i) * 32] = e[i];
         }
 #pragma unroll
         for (int i = 0; i < NM - 1; ++i)
@@ -623,8 +625,8 @@ struct Lane {
         tmask = mk;
     }
 
-    __device__ __forceinline__ T mir_d(int i) const { return mir[i]; }
-    __device__ __forceinline__ T mir_e(int i) const { return mir[NM + i]; }
+    __device__ __forceinline__ T mir_d(int i) const { return mir[i * 32]; }
+    __device__ __forceinline__ T mir_e(int i) const { return mir[(NM + i) * 32]; }
 
     // Settle the lane: advance past converged eigenvalues and blocks until
     // the lane has a task (2x2 solve or sweep), is done, or has exhausted
@@ -872,7 +874,7 @@ __global__ void lane_kernel(KParams p)
     using LaneT = Lane<T, NM, KEXIT>;
     LaneT L;
     L.mir = reinterpret_cast<T *>(reinterpret_cast<char *>(smem_raw) + kQBytesPerLane * blockDim.x) +
-            threadIdx.x * LaneT::MIRROR_PITCH;
+            (threadIdx.x >> 5) * LaneT::MIRROR_WARP_ELEMS + (threadIdx.x & 31);
     L.load(p, b, live);
     QT Q;
     if constexpr (WANTZ) {

@@ -93,14 +93,14 @@ struct QApplier {
 };
 
 // Shared-memory layout of one block (P pairs, 32 lanes each):
-//   mirror   : 2 * NM + 1 floats per chase lane         (Lane::mir)
+//   mirror   : 2 * NM floats per chase lane, per warp [entry][lane]
 //   rot      : [pair][parity][NM][32] float2             (recorded passes)
 //   ctrl     : [pair][parity] int2 (rhi, rlo); rhi < 0 ends the loop
 //   handoff  : per chase lane: zmask, revmask, status, n and pos[NM] bytes
 template <int NM>
 struct SplitSmem {
     static constexpr int P = kSplitPairs;
-    static constexpr size_t mirror = (2ull * NM + 1) * sizeof(float) * 32 * P;
+    static constexpr size_t mirror = 2ull * NM * sizeof(float) * 32 * P;
     static constexpr size_t rot = size_t(P) * 2 * NM * 32 * sizeof(float2);
     static constexpr size_t ctrl = size_t(P) * 2 * sizeof(int2);
     static constexpr size_t hand = size_t(P) * 32 * (4 * sizeof(int) + NM);
@@ -135,7 +135,7 @@ __global__ void __maxnreg__(128) split_kernel(KParams p)
 
     if (chase) {
         Lane<float, NM, KEXIT> L;
-        L.mir = reinterpret_cast<float *>(sm) + slot * Lane<float, NM, KEXIT>::MIRROR_PITCH;
+        L.mir = reinterpret_cast<float *>(sm) + pair * Lane<float, NM, KEXIT>::MIRROR_WARP_ELEMS + lane;
         L.load(p, b, live);
         hand[0 * 32 * P + slot] = (int)L.zmask;
         hand[1 * 32 * P + slot] = (int)L.revmask;

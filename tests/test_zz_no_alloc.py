@@ -16,7 +16,8 @@ from tests.gpu_helpers import orth_err, run_gpu, tri_residual
 
 pytestmark = pytest.mark.gpu
 
-CASES = [(np.float64, 12, 3000), (np.float32, 16, 2000), (np.float64, 32, 700), (np.float32, 29, 1100)]
+CASES = [(np.float64, 12, 3000), (np.float32, 16, 2000), (np.float64, 32, 700), (np.float32, 29, 1100),
+         (np.float32, 8, 3000), (np.float64, 5, 2500), (np.float32, 1, 300)]
 
 
 def _noalloc(d, e):
@@ -63,5 +64,8 @@ def test_noalloc_rejects_what_it_cannot_hold():
     assert lib.bstq_solve_noalloc(bstq.F64, bstq.JOBZ_V, 32, 1 << 20, p, p, p, p, None, None) == -4
     # eigenvalues only need no scratch: this entry point is for jobz = V
     assert lib.bstq_solve_noalloc(bstq.F64, bstq.JOBZ_N, 32, 10, p, p, p, p, None, None) == -2
-    # small n keeps Q in registers (no scratch kernel for it)
-    assert lib.bstq_solve_noalloc(bstq.F32, bstq.JOBZ_V, 8, 10, p, p, p, p, None, None) == -10
+    # small n: the static-position kernel keeps Q in registers and has no
+    # scratch variant, so forcing that family is refused (the default runs the
+    # dynamic-position kernel instead)
+    prm = bstq.Params(0, 0, 0, 0, 0, bstq.KERNEL_STATIC)
+    assert lib.bstq_solve_noalloc(bstq.F32, bstq.JOBZ_V, 8, 10, p, p, p, p, None, ctypes.byref(prm)) == -10
