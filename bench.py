@@ -48,7 +48,10 @@ PAGES_BASELINE = 32768 / 450.9e-6
 # keyed by bstq_describe()'s text and the digest of the CUDA sources
 # (kernel_digest()); a changed kernel no longer matches and reports null
 # (profiles/lane_f32_n16_V_batch32768.md).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("lane<f32,16,V,hybrid,flat> tpb=224 grid=147 smem=143360 regs=255 work=131072", "6461c70af1a1ae55"):
+        4.476672e6 + 0.441344e6,
+}
 
 
 def kernel_digest() -> str:
@@ -121,7 +124,9 @@ def read_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons over
+    the headline's load window (untimed load right before the timed steps,
+    then the timed steps)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -136,7 +141,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.index)],
+                 "-lms", "50", "-i", str(self.index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -177,8 +182,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, **params):
-    """Device-side timing of `steps` solves; returns (ms list, d, e, kernel)."""
+def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, min_warm_s=0.0, **params):
+    """Device-side timing of `steps` solves after `warmup` untimed ones (and,
+    with min_warm_s, more untimed solves until that many seconds of load have
+    passed, so that clock samples right before and during the short timed
+    region are taken under load); returns (ms list, d, e, kernel)."""
     import torch
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
     dt = np.float32 if w["dtype"] == "float32" else np.float64
@@ -193,6 +201,12 @@ def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, **param
     desc = bstq.describe(dt, w["jobz"], w["n"], w["batch"], **params)
     times = []
     with torch.cuda.stream(stream):
+        t_end = time.time() + min_warm_s
+        while time.time() < t_end:
+            for _ in range(20):
+                dg.copy_(d0)
+                bstq.solve(dg, eg, jobz=w["jobz"], Q=Q, work=work, stream=stream, **params)
+            torch.cuda.synchronize()
         for it in range(warmup + steps):
             dg.copy_(d0)
             flush.zero_()
@@ -357,7 +371,7 @@ def main():
 
     with ClockSampler(local) as clk:
         ms, d, e, desc = time_workload(HEADLINE, args.steps, args.warmup, barrier, flush, stream,
-                                       seed=rank_seed(rank))
+                                       seed=rank_seed(rank), min_warm_s=0.8)
     clocks = clk.summary()
     mean_ms, total_problems = aggregate(statistics.mean(ms), HEADLINE["batch"], world, tdist, "cuda")
 

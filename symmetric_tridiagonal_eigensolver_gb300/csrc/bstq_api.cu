@@ -118,16 +118,18 @@ int default_sched(int, int) { return SCHED_FLAT; }
 
 // Default kernel family (static positions in registers, or dynamic
 // positions with d and e in shared memory), per (dtype, jobz, n) from
-// measurement on GB300 (batch 32768/65536): float n <= 16 runs faster with
-// the static kernels (f32 n=16 V 0.167 vs 0.298 ms, N 0.088 vs 0.131 ms);
-// double, and float n > 16, with the dynamic ones (f64 n=12 V 1.27 vs
-// 1.44 ms, f64 n=32 V 14.8 vs 21.7 ms, f32 n=32 V 2.48 vs 3.43 ms).
+// measurement on GB300 (batch 32768, one wave):
+//   float: static at every n (n=16 V 0.137 vs 0.30 ms, n=24 V 0.58 vs
+//          0.65 ms, n=32 V 2.26 vs 2.46 ms, n=32 N 0.21 vs 0.39 ms);
+//   double: dynamic at every n (n=4 V 0.111 vs 0.112 ms, n=8 V 0.44 vs
+//          0.53 ms, n=12 V 0.98 vs 1.31 ms, n=12 N 0.49 vs 0.51 ms):
+//          FP64-bound, and the dynamic kernel has no union of position
+//          ranges and a factored Q update.
 int default_family(int dtype, int jobz, int nm)
 {
     (void)jobz;
-    if (dtype == 0)
-        return nm <= 16 ? FAMILY_STATIC : FAMILY_DYNAMIC;
-    return nm <= 8 ? FAMILY_STATIC : FAMILY_DYNAMIC;
+    (void)nm;
+    return dtype == 0 ? FAMILY_STATIC : FAMILY_DYNAMIC;
 }
 
 int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p)

@@ -14,12 +14,12 @@ pytestmark = pytest.mark.gpu
                                   (np.float64, 12), (np.float64, 16), (np.float64, 24), (np.float64, 32)])
 @pytest.mark.parametrize("jobz", [True, False])
 def test_flat_equals_nested(dt, n, jobz):
-    """The flat lockstep and the nested scheduler run the same per-problem
-    operations, so their results are equal (perf_steqr, Lockstep flat
-    solver: bitwise equal on the dump cases)."""
+    """The flat lockstep and the nested scheduler of the static-position
+    kernels run the same per-problem operations, so their results are equal
+    (perf_steqr, Lockstep flat solver: bitwise equal on the dump cases)."""
     d, e, _, _ = inputs.mixed_problems(n, 4096, dt, seed=n)
-    a = run_gpu(d, e, jobz=jobz, scheduler=1)
-    b = run_gpu(d, e, jobz=jobz, scheduler=2)
+    a = run_gpu(d, e, jobz=jobz, scheduler=1, kernel=1)
+    b = run_gpu(d, e, jobz=jobz, scheduler=2, kernel=1)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[2], b[2])
     if jobz:
@@ -30,11 +30,12 @@ def test_flat_equals_nested(dt, n, jobz):
 @pytest.mark.parametrize("dt,n,qs", [(np.float32, 16, 3), (np.float32, 16, 2), (np.float32, 32, 3), (np.float64, 12, 2),
                                      (np.float64, 12, 3), (np.float64, 16, 3)])
 def test_qstore_variants_agree(dt, n, qs):
+    """Q storage policies of the static-position kernels: same eigenvalues."""
     d, e = inputs.normal_problems(n, 5000, dt, seed=7)
     ref = oracle_ref(d, e)
-    a = run_gpu(d, e, qstore=qs)
+    a = run_gpu(d, e, qstore=qs, kernel=1)
     check_parity(d, e, *a, ref, what=f"qstore={qs}")
-    b = run_gpu(d, e)
+    b = run_gpu(d, e, kernel=1)
     np.testing.assert_array_equal(a[0], b[0])
 
 
