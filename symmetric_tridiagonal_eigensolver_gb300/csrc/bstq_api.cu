@@ -22,6 +22,7 @@ struct Plan {
     size_t smem = 0;
     size_t qwork_bytes = 0;
     size_t work_bytes = 0;
+    int ppb = 0;  // problems per block (split-role kernel)
 };
 
 constexpr int kNmList[] = {4, 8, 12, 16, 24, 32};
@@ -92,15 +93,25 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched, in
     return nullptr;
 }
 
-// Default Q storage: registers while a whole Q fits (n <= 12 in float,
-// n <= 8 in double); float n >= 16 keeps 8 rows of Q in registers and
-// streams the rest from shared memory (one wave of 32768 problems stays
-// resident); double streams Q from global scratch (its FP64 pipe, not L1/L2,
-// bounds it).
-int default_qstore(int dtype, int nm)
+// Default Q storage, from measurement on GB300 (batch 32768, one wave):
+//   float n <= 8: whole Q in registers;
+//   float 9 <= n <= 16, flat scheduler: split roles (chase warps record the
+//     rotations, Q warps apply them; n=16 V 0.131 vs 0.138 ms hybrid, n=12 V
+//     0.072 vs 0.077 ms registers);
+//   float n <= 12 otherwise: registers; float n >= 16 otherwise: 8 rows of Q
+//     in registers, the rest streamed from shared memory (one wave of 32768
+//     problems stays resident);
+//   double: registers for n <= 8, else global scratch (its FP64 pipe, not
+//     L1/L2, bounds it).
+int default_qstore(int dtype, int nm, int sched)
 {
-    if (dtype == 0)
+    if (dtype == 0) {
+        if (nm <= 8)
+            return QS_REG;
+        if (nm <= 16 && sched == SCHED_FLAT)
+            return QS_SPLIT;
         return nm <= 12 ? QS_REG : QS_HYBRID;
+    }
     return nm <= 8 ? QS_REG : QS_GLOBAL;
 }
 
@@ -174,10 +185,10 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
             break;
         }
     const int family = (p && p->kernel) ? p->kernel : default_family(dtype, jobz, nm);
-    int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm)) : 0;
+    const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
+    int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm, sched)) : 0;
     if (family == FAMILY_DYNAMIC && jobz)
         qs = QS_GLOBAL;  // the dynamic kernels keep Q in global scratch
-    const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
     pl.k = find_entry(dtype, jobz, nm, qs, sched, family);
     if (!pl.k)
         return -10;
@@ -187,20 +198,29 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         return BSTQ_ERR_NODEVICE;
     }
     if (qs == QS_SPLIT) {
-        // fixed shape: kSplitPairs chase warps + kSplitPairs Q warps per block,
-        // 32 * kSplitPairs problems per block; shared memory as SplitSmem<nm>
-        const int P = kSplitPairs;
-        const int rr = nm <= 12 ? nm : 12;
+        // fixed shape: kSplitPairs chase warps + kSplitPairs Q warps per block
+        // (four warpgroups), up to 32 * kSplitLivePairs problems per block,
+        // spread evenly over the SMs; shared memory as SplitSmem<nm>
+        const int P = kSplitLivePairs;
+        const int rr = nm <= 8 ? nm : 8;
         size_t off = 2ull * nm * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
                      size_t(P) * 32 * (16 + nm);
         off = (off + 15) / 16 * 16;
         pl.smem = off + size_t(P) * 32 * nm * (nm - rr) * 4;
-        pl.tpb = 64 * P;
+        pl.tpb = 64 * kSplitPairs;
         if (p && p->threads_per_block && p->threads_per_block != pl.tpb)
             return -10;
         if (fa.maxThreadsPerBlock < pl.tpb || pl.smem > (size_t)di.max_smem_block)
             return -10;
-        pl.grid = batch > 0 ? (batch + 32 * P - 1) / (32 * P) : 0;
+        // the register hand-over (setmaxnreg) draws on the block's launch
+        // allocation: launch only if the compiled kernel holds all of it
+        if ((long long)fa.numRegs * pl.tpb < 4LL * 32 * (2 * kSplitChaseRegs + 2 * kSplitQRegs))
+            return -10;
+        long long ppb = batch > 0 ? (batch + di.sms - 1) / di.sms : 1;
+        if (ppb > 32LL * P)
+            ppb = 32LL * P;
+        pl.ppb = (int)ppb;
+        pl.grid = batch > 0 ? (batch + ppb - 1) / ppb : 0;
         pl.qwork_bytes = 0;
         pl.work_bytes = align256(size_t(batch) * 4);
         if (pl.work_bytes == 0)
@@ -291,6 +311,7 @@ int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const voi
     const int per_n = (p && p->max_sweeps_per_n) ? p->max_sweeps_per_n : 30;
     kp.budget = per_n * n;
     kp.sort = (p && p->no_sort) ? 0 : 1;
+    kp.ppb = pl.ppb;
     (void)dtype;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
@@ -564,6 +585,7 @@ extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64
     kp.n = n;
     kp.budget = (q.max_sweeps_per_n ? q.max_sweeps_per_n : 30) * n;
     kp.sort = q.no_sort ? 0 : 1;
+    kp.ppb = pl.ppb;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (err != cudaSuccess)

@@ -51,6 +51,7 @@ struct KParams {
     int n;
     int budget;        // sweep budget per problem (max_sweeps_per_n * n)
     int sort;          // 1: ascending output
+    int ppb;           // problems per block (split-role kernel)
 };
 
 // ---------------------------------------------------------------------------

@@ -3,7 +3,18 @@
 // The static-position kernel runs the bulge chase and the eigenvector update
 // of a problem in the same thread, so the long dependency chain of the chase
 // and the wide, independent eigenvector FMAs share one in-order instruction
-// stream and one register budget.  Here every block holds P pairs of warps.
+// stream and one register budget.  Here every block holds 8 pairs of warps
+// as four warpgroups: warpgroups 0-1 are chase warps, 2-3 their Q partners.
+// The block is launched with 128 registers per thread (the whole register
+// file for 512 threads); the chase warpgroups then give registers back
+// (setmaxnreg.dec to kSplitChaseRegs) and the Q warpgroups take them
+// (setmaxnreg.inc to kSplitQRegs), so a Q lane holds 8 rows of its problem's
+// Q in registers without spilling while the chase keeps what it needs.  The
+// host launches this kernel only after checking that the compiled kernel
+// uses exactly those 128 registers, so the increase always finds its
+// registers.  At most kSplitLivePairs pairs carry problems (shared memory
+// holds seven pairs' state); the eighth pair exits right after the register
+// hand-over.
 // Lane j of chase warp w runs the chase of problem (block, w, j) exactly as
 // bstq_lane.cuh does, but instead of rotating Q it records the pass's
 // rotations (cs, sn) per position in shared memory.  Lane j of the partner Q
@@ -22,7 +33,13 @@
 
 namespace bstq {
 
-constexpr int kSplitPairs = 7;  // 7 chase + 7 Q warps: 224 problems per block
+constexpr int kSplitPairs = 8;      // 8 chase + 8 Q warps: four warpgroups, 512 threads
+constexpr int kSplitLivePairs = 7;  // pairs that carry problems: up to 224 per block
+constexpr int kSplitLaunchRegs = 128;
+constexpr int kSplitChaseRegs = 96;
+constexpr int kSplitQRegs = 160;
+static_assert(4 * 32 * (2 * kSplitChaseRegs + 2 * kSplitQRegs) <= 32 * kSplitPairs * 2 * kSplitLaunchRegs,
+              "register hand-over must fit the launch allocation");
 
 __device__ __forceinline__ void pair_barrier(int id)
 {
@@ -44,12 +61,13 @@ struct QRecorder {
     }
 };
 
-// Rows of Q the Q warp keeps in registers; the rest (a multiple of 4) is
-// streamed from shared memory like the hybrid store.
+// Rows of Q the Q warp keeps in registers (8 rows: 128 registers of the
+// kSplitQRegs); the rest (a multiple of 4) is streamed from shared memory
+// like the hybrid store.
 template <int NM>
 constexpr int split_reg_rows()
 {
-    return NM <= 12 ? NM : 12;
+    return NM <= 8 ? NM : 8;
 }
 
 // Q warp: applies one recorded pass to Q (registers + shared rows).
@@ -92,14 +110,15 @@ struct QApplier {
     }
 };
 
-// Shared-memory layout of one block (P pairs, 32 lanes each):
+// Shared-memory layout of one block (P = kSplitLivePairs pairs, 32 lanes
+// each):
 //   mirror   : 2 * NM floats per chase lane, per warp [entry][lane]
 //   rot      : [pair][parity][NM][32] float2             (recorded passes)
 //   ctrl     : [pair][parity] int2 (rhi, rlo); rhi < 0 ends the loop
 //   handoff  : per chase lane: zmask, revmask, status, n and pos[NM] bytes
 template <int NM>
 struct SplitSmem {
-    static constexpr int P = kSplitPairs;
+    static constexpr int P = kSplitLivePairs;
     static constexpr size_t mirror = 2ull * NM * sizeof(float) * 32 * P;
     static constexpr size_t rot = size_t(P) * 2 * NM * 32 * sizeof(float2);
     static constexpr size_t ctrl = size_t(P) * 2 * sizeof(int2);
@@ -113,27 +132,35 @@ struct SplitSmem {
 };
 
 template <int NM, int SCHED>
-__global__ void __maxnreg__(128) split_kernel(KParams p)
+__global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams p)
 {
     static_assert(SCHED == SCHED_FLAT, "the split kernel pairs warps per pass");
     extern __shared__ uint4 smem_raw[];
     using SM = SplitSmem<NM>;
-    constexpr int P = kSplitPairs;
+    constexpr int P = kSplitLivePairs;  // stride of the per-lane shared arrays
     constexpr int KEXIT = 4;
     char *sm = reinterpret_cast<char *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool chase = warp < P;
-    const int pair = chase ? warp : warp - P;
+    const bool chase = warp < kSplitPairs;
+    const int pair = chase ? warp : warp - kSplitPairs;
+    // no problems for this pair: both of its warps leave right after the
+    // register hand-over (which every warp of a warpgroup executes)
+    const bool idle = pair >= kSplitLivePairs || pair * 32 >= p.ppb;
     const int slot = pair * 32 + lane;  // chase-lane index within the block
-    const long long b = (long long)blockIdx.x * (32 * P) + slot;
-    const bool live = b < p.batch;
+    const long long b = (long long)blockIdx.x * p.ppb + slot;
+    const bool live = slot < p.ppb && b < p.batch;
     float2 *rot = reinterpret_cast<float2 *>(sm + SM::off_rot) + (size_t)pair * 2 * NM * 32 + lane;
     int2 *ctrl = reinterpret_cast<int2 *>(sm + SM::off_ctrl) + pair * 2;
     int *hand = reinterpret_cast<int *>(sm + SM::off_hand);  // [4][32 P] ints
     unsigned char *hpos = reinterpret_cast<unsigned char *>(hand + 4 * 32 * P) + slot;  // [NM][32 P]
     const int bar = 1 + pair;
 
+    // Each role changes its register budget inside its own branch, so the
+    // compiler allocates each role's code under that role's budget.
     if (chase) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kSplitChaseRegs) : "memory");
+        if (idle)
+            return;
         Lane<float, NM, KEXIT> L;
         L.mir = reinterpret_cast<float *>(sm) + pair * Lane<float, NM, KEXIT>::MIRROR_WARP_ELEMS + lane;
         L.load(p, b, live);
@@ -207,6 +234,9 @@ __global__ void __maxnreg__(128) split_kernel(KParams p)
         hand[2 * 32 * P + slot] = L.status;
         pair_barrier(bar);  // output permutation ready
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kSplitQRegs) : "memory");
+        if (idle)
+            return;
         pair_barrier(bar);  // start
         const unsigned zmask = (unsigned)hand[0 * 32 * P + slot];
         const unsigned revmask = (unsigned)hand[1 * 32 * P + slot];
