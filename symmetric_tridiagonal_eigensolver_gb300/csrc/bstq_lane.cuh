@@ -405,6 +405,7 @@ struct Lane {
     int jtot, budget;
     int task, m;
     T f, g;        // running pair of the chase
+    T rpend;       // r of the previous position, not yet stored (float)
     T f0, g0;      // seed of the current sweep, (d_m - mu, e_{m-1})
     T cs2, sn2;    // rotation of a pending 2x2 solve
     unsigned zeroed;  // off-diagonals set to zero by the deflation test
@@ -478,7 +479,7 @@ struct Lane {
         revmask = 0;
         iscale = 0;
         pre = sc = aeff = anorm = T(1);
-        f = g = f0 = g0 = cs2 = sn2 = T(0);
+        f = g = f0 = g0 = cs2 = sn2 = rpend = T(0);
         zeroed = 0;
         clear_pass();
         if (!live) {
@@ -740,8 +741,108 @@ struct Lane {
 
     // Position C of a pass: rotation on the pair (C, C-1) for lanes whose
     // task covers C, identity (lartg of (1, 0)) for the others.
-    template <int C, class QT>
+    template <int C, bool DEFER, class QT>
     __device__ __forceinline__ void chase_at(QT &Q)
+    {
+        if constexpr (sizeof(T) == 4)
+            chase_at_f32<C, DEFER>(Q);
+        else
+            chase_at_f64<C>(Q);
+    }
+
+    // The tail of position C: e_C takes r where the lane's sweep continues
+    // below C, and entry C is final (mirror and deflation test).  In a
+    // static pass (DEFER) the tail of C runs at the start of position C-1,
+    // or when the pass ends: a pass may end at every group boundary, which
+    // ends a basic block, and the tail's late operands would otherwise hold
+    // up the next group's dependency chain.
+    template <int C>
+    __device__ __forceinline__ void finish_at()
+    {
+        if constexpr (sizeof(T) == 4 && C >= 1 && C <= NM - 1) {
+            e[C] = ((m_er >> C) & 1u) ? rpend : e[C];
+            settle_entry<C>();
+        }
+    }
+
+    // float.  The rotation of position C comes from the running pair (f, g)
+    // that position C+1 produced, and position C produces the pair of C-1:
+    // that recurrence is the serial chain of a pass, so it is written to be
+    // short.  With fs, gs the pair scaled so that max(|fs|, |gs|) is in
+    // [1, 1.125] and r2 = fs^2 + gs^2 (c = fs/sqrt(r2), s = gs/sqrt(r2)), the
+    // EXP update of the off-diagonal (page "algo_steqr") is
+    //   e+ = (c^2 - s^2) e + c s (d' - d)
+    //      = ((fs^2 - gs^2) e + fs gs (d' - d)) / r2,
+    // so the next f needs 1/r2 (one Newton step on y0^2, y0 = rsqrt.approx
+    // r2, the flush-to-zero form: its operand is normal, and it measured 19
+    // cycles of latency against 40 for the form that accepts subnormals)
+    // but neither c nor s; the next bulge is s e'' = (gs e'') y.
+    // Everything else (d+, d'+, the eigenvector update, r) uses c and s.
+    //   scale:  2^-k from the exponent field costs a mask and a subtract;
+    //           subtracting the raw bits from those of 2^127 gives a factor
+    //           within 1.125 of it in one integer subtract (the rotation is
+    //           invariant to the scale, and r = f c + g s needs none);
+    //   floor:  r2 gets 2^-100 added, which a normal pair (r2 >= 1) rounds
+    //           away, so f = g = 0 yields a finite 1/r2;
+    //   exact identity: where g = 0 (and for lanes without a rotation at C,
+    //           which run lartg(1, 0)) c = 1, s = 0 are selected and e+ takes
+    //           e through masks, so d, e and Q keep their values bit for bit.
+    template <int C, bool DEFER, class QT>
+    __device__ __forceinline__ void chase_at_f32(QT &Q)
+    {
+        if constexpr (DEFER)
+            finish_at<C + 1>();
+        const bool act = (m_act >> C) & 1u;
+        const bool a22 = (m_22 >> C) & 1u;
+        const bool first = (m_first >> C) & 1u;
+        // one select on the chain: the running pair, or the sweep's seed at
+        // its first position, or (1, 0) where the lane has no rotation
+        const bool own = act && !first;
+        const float fa = own ? f : (first ? f0 : 1.0f);
+        const float ga = own ? g : (first ? g0 : 0.0f);
+        const float mx = fmaxf(fabsf(fa), fabsf(ga));
+        const float sc = __uint_as_float(0x7f000000u - __float_as_uint(mx));
+        const float fs = fa * sc, gs = ga * sc;
+        const float gg = fmaf(gs, gs, 0x1p-100f);
+        const float r2 = fmaf(fs, fs, gg);
+        float y0;
+        asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(r2));  // r2 >= 2^-100: normal
+        const float z2 = y0 * y0;             // ~ 1/r2
+        const float ee = fmaf(-r2, z2, 1.0f);  // 1 - r2 y0^2
+        const float y = fmaf(0.5f * y0, ee, y0);  // 1/sqrt(r2), one Newton step
+        const bool z = ga == 0.0f;
+        const bool idn = z && !a22;
+        float cs = fs * y, sn = gs * y;
+        cs = a22 ? cs2 : (z ? 1.0f : cs);
+        sn = a22 ? sn2 : sn;
+        const float a = d[C], b = e[C - 1], cc = d[C - 1];
+        // e+ from 1/r2 (the chain), exactly e where g = 0
+        const float d1 = fmaf(fs, fs, -gg);
+        const float nn = fmaf(d1, z ? 0.0f : b, (fs * gs) * (cc - a));
+        const float nz = nn * z2;
+        const float en = fmaf(nz, ee, nz + (z ? b : 0.0f));
+        // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP):
+        // d_C from its explicit formula, d_{C-1} from the trace
+        const float p1 = fmaf(cs, a, sn * b);
+        const float p2 = fmaf(cs, b, sn * cc);
+        const float dn = fmaf(cs, p1, sn * p2);
+        d[C] = dn;
+        d[C - 1] = idn ? cc : (a + cc) - dn;
+        rpend = fmaf(fa, cs, ga * sn);
+        e[C - 1] = a22 ? 0.0f : en;
+        if constexpr (C >= 2) {
+            const float eo = e[C - 2];
+            g = (gs * eo) * y;  // new bulge s e''
+            e[C - 2] = cs * eo;
+        }
+        f = en;
+        if constexpr (!DEFER)
+            finish_at<C>();
+        Q.template rot<C>(cs, sn, (m_touch >> C) & 1u);
+    }
+
+    template <int C, class QT>
+    __device__ __forceinline__ void chase_at_f64(QT &Q)
     {
         const bool in = (m_in >> C) & 1u;
         const bool act = (m_act >> C) & 1u;
@@ -754,24 +855,15 @@ struct Lane {
         cs = a22 ? cs2 : cs;
         sn = a22 ? sn2 : sn;
         const T a = d[C], b = e[C - 1], cc = d[C - 1];
-        // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP)
+        // T+ = G^T T G on rows/columns (C, C-1) (page "algo_steqr", EXP);
+        // d_{C-1} from the trace identity and a select (the integer pipe is
+        // idle next to FP64)
         const T p1 = fma(cs, a, sn * b);
         const T p2 = fma(cs, b, sn * cc);
         const T dn = fma(cs, p1, sn * p2);
         const T en = fma(cs, p2, -sn * p1);
-        if constexpr (sizeof(T) == 4) {
-            // float: every entry from its explicit formula, which the
-            // identity rotation reproduces exactly (up to the sign of a zero)
-            const T q1 = fma(cs, cc, -sn * b);
-            const T q2 = fma(cs, b, -sn * a);
-            d[C] = dn;
-            d[C - 1] = fma(cs, q1, -sn * q2);
-        } else {
-            // double: trace identity for d_{C-1} and a select (the integer
-            // pipe is idle next to FP64)
-            d[C] = in ? dn : a;
-            d[C - 1] = in ? (a + cc) - dn : cc;
-        }
+        d[C] = in ? dn : a;
+        d[C - 1] = in ? (a + cc) - dn : cc;
         e[C - 1] = a22 ? T(0) : en;
         e[C] = ((m_er >> C) & 1u) ? r : e[C];
         if constexpr (C >= 2) {
@@ -795,10 +887,11 @@ struct Lane {
         int last = 0;
 #define BSTQ_POS(C)                                                          \
     if constexpr (C <= NM - 1) {                                             \
-        chase_at<C>(Q);                                                      \
+        chase_at<C, true>(Q);                                                \
         if constexpr (C > 1 && ((C - 1) % KEXIT) == 0) {                     \
             if (C - 1 < rlo) {                                               \
                 last = C - 1;                                                \
+                finish_at<C>();                                              \
                 settle_entry<C - 1>();                                       \
                 settle_entry<C - 2>();                                       \
                 goto pass_done;                                              \
@@ -808,6 +901,7 @@ struct Lane {
         BSTQ_GROUPED_SWITCH(KEXIT, group_case<NM>(top), BSTQ_POS)
 #undef BSTQ_POS
         last = 0;
+        finish_at<1>();
         settle_entry<0>();
     pass_done:
         Q.end(last, (m_touch >> last) & 1u);
@@ -819,7 +913,7 @@ struct Lane {
     {
         if constexpr (C >= 1) {
             if (C <= hi_l && C >= lo_l)
-                chase_at<C>(Q);
+                chase_at<C, false>(Q);
             own_positions<C - 1>(Q);
         }
     }

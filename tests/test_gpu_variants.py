@@ -44,8 +44,10 @@ def test_block_size_does_not_change_results(tpb):
     """Block size changes the launch shape only (perf_steqr, Work-group
     multiplier: byte-identical outputs)."""
     d, e = inputs.normal_problems(16, 3000, np.float32, seed=8)
-    a = run_gpu(d, e, threads_per_block=tpb)
-    b = run_gpu(d, e)
+    # the hybrid store takes any block size (the split-role kernel has a
+    # fixed 512-thread shape and rejects others)
+    a = run_gpu(d, e, threads_per_block=tpb, qstore=4)
+    b = run_gpu(d, e, qstore=4)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
 
@@ -86,9 +88,13 @@ def test_streams_are_honoured():
 
 def test_oversized_block_is_rejected_not_launched():
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
-    # 256 threads x 1 KiB of shared Q exceeds what one block may hold
+    # 1024 threads x 512 B of shared Q rows exceeds what one block may hold
     with pytest.raises(bstq.BstqError) as ei:
-        run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), threads_per_block=1024)
+        run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), threads_per_block=1024, qstore=4)
+    assert ei.value.code == -10
+    # the split-role kernel has one block shape (512 threads)
+    with pytest.raises(bstq.BstqError) as ei:
+        run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), threads_per_block=256, qstore=5)
     assert ei.value.code == -10
 
 
