@@ -574,6 +574,7 @@ __global__ void dyn_kernel(KParams p)
             dout[pos[s]] = dv[s];
     if constexpr (WANTZ) {
         using Q_ = DynQ<T, NM>;
+        const bool vec = q_vector_ok<T>(p.Q, n);
         for (int s = 0; s < n; ++s) {
             typename Q_::E x[Q_::NE];
             L.q.load(s, x);
@@ -588,11 +589,12 @@ __global__ void dyn_kernel(KParams p)
             T scale = T(1);
             if constexpr (LaneT::FASTQ)
                 scale = L.sdl[s * tpb];  // Q = Qt diag(delta)
-            T *qc = qout + (long long)ps * n;
+            if constexpr (LaneT::FASTQ) {
 #pragma unroll
-            for (int r = 0; r < NM; ++r)
-                if (r < n)
-                    qc[r] = LaneT::FASTQ ? col[r] * scale : col[r];
+                for (int r = 0; r < Q_::NR; ++r)
+                    col[r] *= scale;
+            }
+            store_col(qout + (long long)ps * n, col, n, vec);
         }
     }
     p.info[b] = (L.status == ST_FAIL) ? L.info : 0;

@@ -226,6 +226,45 @@ struct QMix {
     }
 };
 
+// One column of Q (rows 0 .. n-1) to global memory at qc.  With vec set the
+// column is written in 16-byte vectors: a lane owns a whole problem, so the
+// 32 lanes of a warp store to 32 places far apart, and each store
+// instruction costs the memory pipeline one request per lane whatever its
+// width; 16-byte stores take a quarter of the requests of 4-byte ones (for
+// float).  vec requires n * sizeof(T) to be a multiple of 16 and Q to start
+// on a 16-byte boundary, so that every column does (q_vector_ok).
+template <typename T, int R>
+__device__ __forceinline__ void store_col(T *qc, const T (&col)[R], int n, bool vec)
+{
+    constexpr int W = 16 / (int)sizeof(T);
+    if (vec) {
+        struct alignas(16) V {
+            T x[W];
+        };
+#pragma unroll
+        for (int v = 0; v < R / W; ++v) {
+            if (v * W < n) {
+                V o;
+#pragma unroll
+                for (int k = 0; k < W; ++k)
+                    o.x[k] = col[v * W + k];
+                reinterpret_cast<V *>(qc)[v] = o;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (r < n)
+                qc[r] = col[r];
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ bool q_vector_ok(const void *Q, int n)
+{
+    return ((n * (int)sizeof(T)) % 16) == 0 && ((reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+}
+
 // Empty store for eigenvalues only.
 template <typename T, int NM>
 struct QNone {
@@ -1058,16 +1097,13 @@ __global__ void lane_kernel(KParams p)
         if (s < n)
             dout[pos[s]] = L.d[s];
     if constexpr (WANTZ) {
+        const bool vec = q_vector_ok<T>(p.Q, n);
 #pragma unroll
         for (int s = 0; s < NM; ++s) {
             if (s < n) {
                 T col[QFor<T, NM, WANTZ, QS>::ROWS];
                 Q.get_col(s, col);
-                T *qc = qout + (long long)pos[s] * n;
-#pragma unroll
-                for (int r = 0; r < NM; ++r)
-                    if (r < n)
-                        qc[r] = col[r];
+                store_col(qout + (long long)pos[s] * n, col, n, vec);
             }
         }
     }

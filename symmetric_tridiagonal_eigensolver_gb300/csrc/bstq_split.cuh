@@ -271,16 +271,13 @@ __global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams 
                 for (int i = 0; i < n * n; ++i)
                     qout[i] = __int_as_float(0x7fffffff);
             } else {
+                const bool vec = q_vector_ok<float>(p.Q, n);
 #pragma unroll
                 for (int s = 0; s < NM; ++s) {
                     if (s < n) {
                         float col[NM];
                         A.Q.get_col(s, col);
-                        float *qc = qout + (long long)hpos[s * 32 * P] * n;
-#pragma unroll
-                        for (int r = 0; r < NM; ++r)
-                            if (r < n)
-                                qc[r] = col[r];
+                        store_col(qout + (long long)hpos[s * 32 * P] * n, col, n, vec);
                     }
                 }
             }

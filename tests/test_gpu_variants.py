@@ -143,3 +143,27 @@ def test_split_role_kernel(n):
     d[7, 3] = np.inf
     c = run_gpu(d, e, qstore=5, max_sweeps_per_n=1)
     assert c[2][7] == -1 and np.all(np.isnan(c[1][7]))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt,n,params", [(np.float32, 16, {}), (np.float32, 16, {"qstore": 4}),
+                                         (np.float32, 8, {}), (np.float64, 12, {})])
+def test_unaligned_q_matches_aligned(dt, n, params):
+    """Q columns go out in 16-byte vectors when Q starts on a 16-byte boundary
+    and n * sizeof(T) is a multiple of 16; a Q that is only element-aligned
+    takes the element-wise stores and must give the same bytes."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    d, e = inputs.normal_problems(n, 1000, dt, seed=21)
+    ref = run_gpu(d, e, **params)
+    dev = torch.device("cuda:0")
+    dg = torch.from_numpy(d.copy()).to(dev)
+    eg = torch.from_numpy(e.copy()).to(dev)
+    buf = torch.full((1000 * n * n + 1,), float("nan"), dtype=dg.dtype, device=dev)
+    Q = buf[1:].view(1000, n, n)
+    assert Q.data_ptr() % 16 != 0
+    lam, Qo, info = bstq.solve(dg, eg, jobz=True, Q=Q, **params)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(lam.cpu().numpy(), ref[0])
+    np.testing.assert_array_equal(Qo.cpu().numpy(), ref[1])
+    np.testing.assert_array_equal(info.cpu().numpy(), ref[2])
