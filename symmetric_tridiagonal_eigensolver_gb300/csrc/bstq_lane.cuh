@@ -113,7 +113,10 @@ struct El<double> {
 // lane-major layout with an odd lane pitch, whose addresses are compile-time
 // offsets, measured slower for the hybrid store.)  Loads are unconditional
 // (every lane's region holds finite values).
-template <typename T, int NM, int RR, int MR>
+// ST > 0 fixes the stride (in vectors) at compile time: the compiler then
+// knows that the column a position loads is not the one the previous
+// position stored, and can issue the load ahead of the store.
+template <typename T, int NM, int RR, int MR, int ST = 0>
 struct QMix {
     using Tr = El<T>;
     using E = typename Tr::E;
@@ -139,7 +142,7 @@ struct QMix {
         base = reinterpret_cast<V16 *>(p);
         stride = s;
     }
-    __device__ __forceinline__ int vidx(int k, int g) const { return (k * G + g) * stride; }
+    __device__ __forceinline__ int vidx(int k, int g) const { return (k * G + g) * (ST > 0 ? ST : stride); }
     __device__ __forceinline__ void load(int k, E (&x)[NEM > 0 ? NEM : 1]) const
     {
 #pragma unroll

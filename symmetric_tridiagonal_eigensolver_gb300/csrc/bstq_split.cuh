@@ -71,16 +71,22 @@ constexpr int split_reg_rows()
 }
 
 // Q warp: applies one recorded pass to Q (registers + shared rows).
+// The shared rows use the block's fixed lane stride (32 lanes per live pair),
+// and each position's rotation is read one position ahead, before the
+// position's store, so neither shared-memory read waits behind a store.
 template <int NM, int KEXIT>
 struct QApplier {
     static constexpr int RR = split_reg_rows<NM>();
-    QMix<float, NM, RR, NM - RR> Q;
+    QMix<float, NM, RR, NM - RR, 32 * kSplitLivePairs> Q;
     const float2 *buf;
+    float2 rn;  // rotation of the next position
 
     template <int C>
     __device__ __forceinline__ void apply_at()
     {
-        const float2 r = buf[C * 32];
+        const float2 r = rn;
+        if constexpr (C >= 2)
+            rn = buf[(C - 1) * 32];
         Q.template rot<C>(r.x, r.y, true);
     }
 
@@ -90,6 +96,7 @@ struct QApplier {
     __device__ __forceinline__ void pass(int rhi, int rlo)
     {
         const int top = group_top<NM, KEXIT>(rhi);
+        rn = buf[top * 32];
         Q.begin(top);
         int last = 0;
 #define BSTQ_APOS(C)                                                         \
