@@ -47,10 +47,10 @@ PAGES_BASELINE = 32768 / 450.9e-6
 # DRAM bytes (read + write) per launch measured by ncu for a kernel variant,
 # keyed by bstq_describe()'s text and the digest of the CUDA sources
 # (kernel_digest()); a changed kernel no longer matches and reports null
-# (profiles/lane_f32_n16_V_batch32768.md).
+# (profiles/split_f32_n16_V_batch32768.md).
 NCU_TRAFFIC = {
-    ("lane<f32,16,V,hybrid,flat> tpb=224 grid=147 smem=143360 regs=255 work=131072", "6461c70af1a1ae55"):
-        4.476672e6 + 0.441344e6,
+    ("lane<f32,16,V,split,flat> tpb=512 grid=152 smem=207984 regs=128 work=131072", "cb4cccc46dcf2b9d"):
+        4.2752e6 + 0.144384e6,
 }
 
 
