@@ -95,11 +95,14 @@ class Result:
 
 
 def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
-          sort: bool = True, nthreads: int = 1, lib=None) -> Result:
+          sort: bool = True, nthreads: int = 1, lib=None, Z=None) -> Result:
     """Run the oracle on host arrays ``d`` (batch, n) and ``e`` (batch, n-1).
 
     The dtype of ``d`` (float32 or float64) selects the precision; ``e`` is
-    cast to it.  Inputs are not modified."""
+    cast to it.  With ``Z`` (batch, n, n) given (and jobz), the rotations are
+    right-applied to Z instead of the identity (back_transform, BatchLAS page
+    "algo_steqr", eigenvector accumulation): ``Q`` is then Z times the
+    eigenvectors.  Inputs are not modified."""
     d = np.asarray(d)
     if d.dtype not in (np.float32, np.float64):
         raise TypeError("oracle: d must be float32 or float64")
@@ -111,11 +114,16 @@ def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
     lam = np.ascontiguousarray(d, dtype=dt).copy()
     ec = np.ascontiguousarray(e, dtype=dt)
     Qc = np.empty((batch, n, n), dtype=dt) if jobz else None  # column-major per problem
+    mode = int(bool(jobz))
+    if jobz and Z is not None:
+        Zc = np.asarray(Z, dtype=dt).reshape(batch, n, n)
+        Qc[...] = np.swapaxes(Zc, 1, 2)  # memory [b][j][i] = Z_ij
+        mode = 2
     info = np.zeros(batch, dtype=np.int32)
     cnt = np.zeros(3, dtype=np.int64)
     lib = lib if lib is not None else _load()
     fn = lib.oracle_steqr_batch_f32 if dt == np.float32 else lib.oracle_steqr_batch_f64
-    rc = fn(int(n), int(batch), int(bool(jobz)), int(maxit_per_n), int(bool(sort)),
+    rc = fn(int(n), int(batch), mode, int(maxit_per_n), int(bool(sort)),
             lam.ctypes.data, ec.ctypes.data if ec.size else None,
             Qc.ctypes.data if jobz else None, info.ctypes.data, cnt.ctypes.data,
             int(nthreads))

@@ -91,7 +91,9 @@ static int FN(eidx)(FN(view_t) v, int p)
 /*
  * Solve one problem.  d[n] is overwritten with the eigenvalues; e_in[n-1] is
  * read only; ework[n] is scratch; Q[n*n] (column-major, used iff jobz != 0)
- * receives the eigenvectors.  cnt[0..2] accumulate (implicit steps,
+ * receives the eigenvectors (jobz == 1), or holds a basis Z on entry and
+ * receives Z times the eigenvectors (jobz == 2, back_transform).
+ * cnt[0..2] accumulate (implicit steps,
  * rotations, 2x2 direct solves).  Returns info: 0 converged, k > 0 the sweep
  * budget ran out with k off-diagonals still nonzero, -1 non-finite input.
  */
@@ -123,8 +125,9 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort,
     for (i = 0; i + 1 < n; ++i)
         e[i] = e_in[i];
     /* algo_steqr, eigenvector accumulation: back_transform = false starts
-     * from Q = I. */
-    if (jobz)
+     * from Q = I (jobz == 1); back_transform = true (jobz == 2) takes the
+     * caller's Q as the basis the rotations are right-applied to. */
+    if (jobz == 1)
         for (i = 0; i < n * n; ++i)
             Q[i] = (i % (n + 1) == 0) ? (real_t)1 : (real_t)0;
 

@@ -101,3 +101,18 @@ def problems(kind: str, n: int, batch: int, dtype, seed: int = 0):
         d, e, _, _ = mixed_problems(n, batch, dtype, seed)
         return d, e
     raise ValueError(f"unknown input kind {kind!r}")
+
+
+def orthogonal_bases(n: int, batch: int, dtype, seed: int = 0):
+    """Z (batch, n, n) with Z[b] orthogonal (to the dtype's rounding): the Q
+    factor of a matrix of i.i.d. N(0,1) entries (numpy's QR in float64),
+    columns signed so that R has a positive diagonal, rounded to dtype.  Used
+    as the basis Z of the back_transform case (Q on exit = Z times the
+    eigenvectors)."""
+    dt = _as_dtype(dtype)
+    rng = np.random.default_rng(seed)
+    G = rng.standard_normal((batch, n, n))
+    Qf, R = np.linalg.qr(G)
+    sgn = np.sign(np.diagonal(R, axis1=1, axis2=2))
+    sgn[sgn == 0] = 1.0
+    return (Qf * sgn[:, None, :]).astype(dt)

@@ -101,3 +101,18 @@ def toeplitz_eigenvalues(n, a, b):
     pi = np.longdouble("3.14159265358979323846264338327950288")
     v = np.longdouble(a) + 2 * np.longdouble(b) * np.cos(k * pi / (n + 1))
     return np.sort(v)
+
+
+def back_residual_orth(d, e, Z, lam, V):
+    """For back_transform output V = Z Q: max |A V - V Lambda| with
+    A = Z T Z^T, and max |V^T V - I|, per problem, in long double."""
+    T = dense(d, e, np.longdouble)
+    Zl = np.asarray(Z, dtype=np.longdouble)
+    A = Zl @ T @ np.swapaxes(Zl, 1, 2)
+    Vl = np.asarray(V, dtype=np.longdouble)
+    L = np.asarray(lam, dtype=np.longdouble)
+    n = T.shape[-1]
+    R = A @ Vl - Vl * L[:, None, :]
+    O = np.swapaxes(Vl, 1, 2) @ Vl - np.eye(n, dtype=np.longdouble)
+    return (np.abs(R).reshape(len(T), -1).max(axis=1).astype(np.float64),
+            np.abs(O).reshape(len(T), -1).max(axis=1).astype(np.float64))

@@ -40,6 +40,7 @@ MUTATIONS = [
     ("budget_off_by_all", "if (jtot == budget) {", "if (jtot == budget + 1000000) {"),
     ("block_ignores_exact_zero", "while (le < n - 1 && e[le] != (real_t)0)",
      "while (le < n - 1 && e[le] != (real_t)-12345)"),
+    ("back_transform_ignored", "    if (jobz == 1)\n", "    if (jobz >= 1)\n"),
 ]
 
 
@@ -109,6 +110,17 @@ def pin_failures(lib):
         rel = np.abs((r.lam.astype(np.float64) - ref) / ref).max(1)
         check("graded_rate", r.sweeps <= 1.5 * 16 * 100)
         check("graded_relacc", np.median(rel) <= 100 * eps)
+        # back_transform: the rotations are right-applied to an orthogonal Z,
+        # so Z Q holds the eigenvectors of Z T Z^T
+        d, e = inputs.normal_problems(7, 20, dt, seed=6)
+        Z = inputs.orthogonal_bases(7, 20, dt, seed=6)
+        r = oracle.steqr(d, e, jobz=True, Z=Z, lib=lib)
+        tn = H.norm1(d, e).astype(np.float64)
+        if np.all(np.isfinite(r.Q)):
+            res, orth = H.back_residual_orth(d, e, Z, r.lam, r.Q)
+            check("back_res", np.all(res <= 64 * 7 * eps * tn))
+        else:
+            bad.append("back_finite")
     return bad
 
 

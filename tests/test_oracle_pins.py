@@ -367,3 +367,55 @@ def test_multithreaded_batch_matches_single_thread():
     b = oracle.steqr(d, e, jobz=True, nthreads=4)
     assert np.array_equal(a.lam, b.lam) and np.array_equal(a.Q, b.Q)
     assert (a.sweeps, a.rotations, a.solves2x2) == (b.sweeps, b.rotations, b.solves2x2)
+
+
+# --- back_transform (BatchLAS page "algo_steqr", eigenvector accumulation:
+# with back_transform the rotations are right-applied to the caller's basis
+# instead of the identity) ---
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_back_transform_identity_basis_is_bitwise_plain(dt):
+    d, e = inputs.normal_problems(11, 50, dt, seed=31)
+    a = oracle.steqr(d, e, jobz=True)
+    b = oracle.steqr(d, e, jobz=True, Z=np.broadcast_to(np.eye(11, dtype=dt), (50, 11, 11)))
+    np.testing.assert_array_equal(a.lam, b.lam)
+    np.testing.assert_array_equal(a.Q, b.Q)
+    np.testing.assert_array_equal(a.info, b.info)
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_back_transform_permutation_basis_permutes_rows_exactly(dt):
+    """Z = P (a row permutation): Z Q has the rows of Q permuted, bit for bit,
+    since each row of the basis is rotated on its own."""
+    n, batch = 9, 40
+    d, e = inputs.normal_problems(n, batch, dt, seed=32)
+    rng = np.random.default_rng(5)
+    perms = np.stack([rng.permutation(n) for _ in range(batch)])
+    P = np.zeros((batch, n, n), dtype=dt)
+    P[np.arange(batch)[:, None], np.arange(n)[None, :], perms] = 1
+    a = oracle.steqr(d, e, jobz=True)
+    b = oracle.steqr(d, e, jobz=True, Z=P)
+    np.testing.assert_array_equal(b.lam, a.lam)
+    np.testing.assert_array_equal(b.Q, np.take_along_axis(a.Q, perms[:, :, None], axis=1))
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+@pytest.mark.parametrize("n", [2, 7, 16, 32])
+def test_back_transform_solves_the_dense_problem(dt, n):
+    """With an orthogonal Z, V = Z Q holds the eigenvectors of A = Z T Z^T:
+    residual and orthogonality within the stated bounds, and V agrees with
+    Z times the plain eigenvectors."""
+    batch = 60
+    d, e = inputs.normal_problems(n, batch, dt, seed=33 + n)
+    Z = inputs.orthogonal_bases(n, batch, dt, seed=n)
+    eps = H.eps_of(dt)
+    tn = H.norm1(d, e).astype(np.float64)
+    r = oracle.steqr(d, e, jobz=True, Z=Z)
+    assert np.all(r.info == 0)
+    res, orth = H.back_residual_orth(d, e, Z, r.lam, r.Q)
+    assert np.all(res <= 64 * n * eps * tn)
+    assert np.all(orth <= 64 * n * eps)
+    plain = oracle.steqr(d, e, jobz=True)
+    np.testing.assert_array_equal(r.lam, plain.lam)
+    zq = Z.astype(np.float64) @ plain.Q.astype(np.float64)
+    assert np.abs(zq - r.Q).max() <= 64 * n * eps
