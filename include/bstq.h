@@ -82,6 +82,14 @@ typedef struct {
     int threads_per_block; /* 0 = chosen by the library; else a multiple of
                               32 in [32, 1024]                               */
     int kernel;            /* bstq_kernel: 0 = chosen per (dtype, jobz, n)   */
+    int back_transform;    /* 0 (default): Q starts as the identity.
+                              1 (jobz == V only): Q is in/out.  On entry it
+                              holds a basis Z per problem (same layout as the
+                              output, Q[b*n*n + j*n + i] = Z_ij); the
+                              rotations are right-applied to it, so on exit
+                              it holds Z times the eigenvectors of T, sorted
+                              with lambda (BatchLAS page "algo_steqr",
+                              eigenvector accumulation: back_transform).     */
 } bstq_params;
 
 /* Kernel family.  STATIC: d and e in registers, the chase unrolled over
@@ -114,7 +122,8 @@ size_t bstq_work_size_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
  *   d     in/out  batch*n values of dtype; on exit the eigenvalues.
  *   e     in      batch*(n-1) values; may be NULL when n == 1.
  *   Q     out     batch*n*n values when jobz == BSTQ_JOBZ_V; ignored (may be
- *                 NULL) when jobz == BSTQ_JOBZ_N.
+ *                 NULL) when jobz == BSTQ_JOBZ_N.  In/out with
+ *                 p->back_transform (the basis Z on entry).
  *   work  in/out  at least bstq_work_size(...) bytes, 16-byte aligned;
  *                 receives int32 info[batch].
  * d, e and Q must be aligned to their element size.
@@ -129,9 +138,10 @@ int bstq_solve_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
                   const bstq_params *p);
 
 /*
- * End-to-end variant on HOST buffers: copies h_d and h_e to the device
- * workspace `dev`, solves there and copies lambda (into h_d), Q (into h_Q,
- * when jobz == V) and info (into h_info) back, all enqueued on `stream`.
+ * End-to-end variant on HOST buffers: copies h_d and h_e (and h_Q with
+ * p->back_transform) to the device workspace `dev`, solves there and copies
+ * lambda (into h_d), Q (into h_Q, when jobz == V) and info (into h_info)
+ * back, all enqueued on `stream`.
  * The host buffers are read/written asynchronously when they are pinned
  * (cudaHostAlloc / cudaHostRegister); the caller synchronises the stream
  * before reading them.  `dev` must hold bstq_host_work_size(...) bytes of

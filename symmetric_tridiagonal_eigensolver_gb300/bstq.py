@@ -33,7 +33,8 @@ class Params(ctypes.Structure):
     """bstq_params; all-zero means the defaults."""
     _fields_ = [("no_sort", ctypes.c_int), ("max_sweeps_per_n", ctypes.c_int),
                 ("scheduler", ctypes.c_int), ("qstore", ctypes.c_int),
-                ("threads_per_block", ctypes.c_int), ("kernel", ctypes.c_int)]
+                ("threads_per_block", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("back_transform", ctypes.c_int)]
 
 
 class BstqError(RuntimeError):
@@ -90,9 +91,10 @@ def load(path: str = LIB_PATH):
         return lib
 
 
-def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0, kernel=0):
+def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0, kernel=0,
+            back_transform=False):
     return Params(int(bool(no_sort)), int(max_sweeps_per_n), int(scheduler), int(qstore),
-                  int(threads_per_block), int(kernel))
+                  int(threads_per_block), int(kernel), int(bool(back_transform)))
 
 
 def _dtype_code(dt) -> int:
@@ -135,13 +137,22 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def solve(d, e, jobz: bool = True, Q=None, work=None, stream=None, **params):
+def solve(d, e, jobz: bool = True, Q=None, work=None, stream=None, Z=None, **params):
     """Solve on CUDA tensors: ``d`` (batch, n) in/out (eigenvalues on exit),
     ``e`` (batch, n-1).  Returns (d, Q, info) where Q is (batch, n, n) with
     Q[b, :, j] the eigenvector of d[b, j] (None for jobz N) and info (batch,)
-    int32.  Work is enqueued on ``stream`` (default: torch's current stream);
-    nothing is synchronised."""
+    int32.  With ``Z`` (batch, n, n) given, the rotations are right-applied to
+    Z (back_transform) and the returned Q is Z times the eigenvectors; ``Q``
+    given with ``back_transform=True`` is read as the basis in the library's
+    storage layout (memory [b][j][i] = Z_ij).  Work is enqueued on ``stream``
+    (default: torch's current stream); nothing is synchronised."""
     import torch
+    if Z is not None:
+        if not jobz:
+            raise ValueError("bstq.solve: Z needs jobz = True")
+        # storage layout of the library: memory [b][j][i] = Z_ij
+        Q = Z.to(device=d.device, dtype=d.dtype).transpose(1, 2).contiguous()
+        params["back_transform"] = True
     if not (d.is_cuda and d.is_contiguous()):
         raise ValueError("bstq.solve: d must be a contiguous CUDA tensor")
     if d.dim() != 2:

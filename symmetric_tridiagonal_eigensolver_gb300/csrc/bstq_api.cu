@@ -164,6 +164,8 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
             return -10;
         if (p->kernel < 0 || p->kernel > 2)
             return -10;
+        if (p->back_transform != 0 && p->back_transform != 1)
+            return -10;
         if (p->threads_per_block != 0 &&
             (p->threads_per_block < 32 || p->threads_per_block > 1024 || p->threads_per_block % 32))
             return -10;
@@ -312,6 +314,7 @@ int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const voi
     kp.budget = per_n * n;
     kp.sort = (p && p->no_sort) ? 0 : 1;
     kp.ppb = pl.ppb;
+    kp.back = (Q && p && p->back_transform) ? 1 : 0;
     (void)dtype;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
@@ -427,6 +430,9 @@ extern "C" int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t 
         return cuda_fail(err, "cudaMemcpyAsync d");
     if (be && (err = cudaMemcpyAsync(de, h_e, be, cudaMemcpyHostToDevice, st)) != cudaSuccess)
         return cuda_fail(err, "cudaMemcpyAsync e");
+    if (bq && p && p->back_transform &&
+        (err = cudaMemcpyAsync(dq, h_Q, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(err, "cudaMemcpyAsync Q (basis)");
     rc = bstq_solve_ex(dtype, jobz, n, batch, dd, de, bq ? dq : nullptr, dw, stream, p);
     if (rc)
         return rc == -10 ? -11 : (rc < 0 ? -9 : rc);
@@ -586,6 +592,7 @@ extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64
     kp.budget = (q.max_sweeps_per_n ? q.max_sweeps_per_n : 30) * n;
     kp.sort = q.no_sort ? 0 : 1;
     kp.ppb = pl.ppb;
+    kp.back = q.back_transform ? 1 : 0;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (err != cudaSuccess)

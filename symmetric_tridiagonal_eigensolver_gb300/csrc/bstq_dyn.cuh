@@ -52,6 +52,18 @@ struct DynQ {
         for (int g = 0; g < G; ++g)
             base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
     }
+    // Column s from the caller's basis: rows 0 .. n-1 of zc, zero below
+    // (back_transform).
+    __device__ __forceinline__ void init_col_from(int s, const T *zc, int n, bool vec) const
+    {
+        T col[NR];
+        load_col(zc, col, n, vec);
+        E x[NE];
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+            x[j] = Tr::pack(&col[j * RPE]);
+        store(s, x);
+    }
     __device__ __forceinline__ void init_col(int s, int row_of_one) const
     {
         E x[NE];
@@ -491,9 +503,16 @@ __global__ void dyn_kernel(KParams p)
     }
     L.load(p, b, live);
     if constexpr (WANTZ) {
+        const T *zb = reinterpret_cast<const T *>(p.Q) + b * (long long)L.n * L.n;
+        const bool zvec = q_vector_ok<T>(p.Q, L.n);
         if (L.status == ST_RUN)
             for (int s = 0; s < NM; ++s) {
-                L.q.init_col(s, s < L.n ? L.phys(s) : s);
+                // column phys(s) of the identity, or of the caller's basis
+                // with back_transform
+                if (p.back && s < L.n)
+                    L.q.init_col_from(s, zb + (long long)L.phys(s) * L.n, L.n, zvec);
+                else
+                    L.q.init_col(s, s < L.n ? L.phys(s) : s);
                 if constexpr (LaneT::FASTQ) {
                     L.sdl[s * tpb] = T(1);
                     L.sil[s * tpb] = T(1);

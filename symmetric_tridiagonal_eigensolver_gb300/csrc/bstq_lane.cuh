@@ -52,6 +52,7 @@ struct KParams {
     int budget;        // sweep budget per problem (max_sweeps_per_n * n)
     int sort;          // 1: ascending output
     int ppb;           // problems per block (split-role kernel)
+    int back;          // 1: Q holds the basis Z on entry (back_transform)
 };
 
 // ---------------------------------------------------------------------------
@@ -83,6 +84,7 @@ struct El<float> {
         return pk2(row == base ? 1.0f : 0.0f, row == base + 1 ? 1.0f : 0.0f);
     }
     __device__ static __forceinline__ void get(E v, float *out) { upk2(v, out[0], out[1]); }
+    __device__ static __forceinline__ E pack(const float *in) { return pk2(in[0], in[1]); }
 };
 
 template <>
@@ -101,7 +103,76 @@ struct El<double> {
     }
     __device__ static __forceinline__ E unit(int row, int base) { return row == base ? 1.0 : 0.0; }
     __device__ static __forceinline__ void get(E v, double *out) { out[0] = v; }
+    __device__ static __forceinline__ E pack(const double *in) { return in[0]; }
 };
+
+// One column of Q (rows 0 .. n-1) to global memory at qc.  With vec set the
+// column is written in 16-byte vectors: a lane owns a whole problem, so the
+// 32 lanes of a warp store to 32 places far apart, and each store
+// instruction costs the memory pipeline one request per lane whatever its
+// width; 16-byte stores take a quarter of the requests of 4-byte ones (for
+// float).  vec requires n * sizeof(T) to be a multiple of 16 and Q to start
+// on a 16-byte boundary, so that every column does (q_vector_ok).
+template <typename T, int R>
+__device__ __forceinline__ void store_col(T *qc, const T (&col)[R], int n, bool vec)
+{
+    constexpr int W = 16 / (int)sizeof(T);
+    if (vec) {
+        struct alignas(16) V {
+            T x[W];
+        };
+#pragma unroll
+        for (int v = 0; v < R / W; ++v) {
+            if (v * W < n) {
+                V o;
+#pragma unroll
+                for (int k = 0; k < W; ++k)
+                    o.x[k] = col[v * W + k];
+                reinterpret_cast<V *>(qc)[v] = o;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (r < n)
+                qc[r] = col[r];
+    }
+}
+
+// One column of the caller's basis Z (rows 0 .. n-1) from global memory into
+// col[]; rows n .. R-1 are zero.  vec as for store_col.
+template <typename T, int R>
+__device__ __forceinline__ void load_col(const T *zc, T (&col)[R], int n, bool vec)
+{
+    constexpr int W = 16 / (int)sizeof(T);
+    if (vec) {
+        struct alignas(16) V {
+            T x[W];
+        };
+#pragma unroll
+        for (int v = 0; v < R / W; ++v) {
+            V o;
+            if (v * W < n)
+                o = reinterpret_cast<const V *>(zc)[v];
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                col[v * W + k] = v * W < n ? o.x[k] : T(0);
+        }
+#pragma unroll
+        for (int r = (R / W) * W; r < R; ++r)
+            col[r] = T(0);
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            col[r] = r < n ? zc[r] : T(0);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ bool q_vector_ok(const void *Q, int n)
+{
+    return ((n * (int)sizeof(T)) % 16) == 0 && ((reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+}
 
 // Q with rows [0, RR) in registers and rows [RR, RR + MR) in memory (shared
 // or global), streamed one column at a time: the column shared by two
@@ -175,6 +246,27 @@ struct QMix {
             store(s, x);
         }
     }
+    // Column s (static s in an unrolled loop) from the caller's basis:
+    // rows 0 .. n-1 of zc, zero below (back_transform).
+    __device__ __forceinline__ void init_col_from(int s, const T *zc, int n, bool vec)
+    {
+        T col[RR + MR];
+        load_col(zc, col, n, vec);
+#pragma unroll
+        for (int k = 0; k < NM; ++k)
+            if (k == s) {
+#pragma unroll
+                for (int j = 0; j < NER; ++j)
+                    qr[k][j] = Tr::pack(&col[j * RPE]);
+            }
+        if constexpr (NEM > 0) {
+            E x[NEM];
+#pragma unroll
+            for (int j = 0; j < NEM; ++j)
+                x[j] = Tr::pack(&col[RR + j * RPE]);
+            store(s, x);
+        }
+    }
     __device__ __forceinline__ void begin(int hi)
     {
         if constexpr (NEM > 0)
@@ -228,45 +320,6 @@ struct QMix {
         }
     }
 };
-
-// One column of Q (rows 0 .. n-1) to global memory at qc.  With vec set the
-// column is written in 16-byte vectors: a lane owns a whole problem, so the
-// 32 lanes of a warp store to 32 places far apart, and each store
-// instruction costs the memory pipeline one request per lane whatever its
-// width; 16-byte stores take a quarter of the requests of 4-byte ones (for
-// float).  vec requires n * sizeof(T) to be a multiple of 16 and Q to start
-// on a 16-byte boundary, so that every column does (q_vector_ok).
-template <typename T, int R>
-__device__ __forceinline__ void store_col(T *qc, const T (&col)[R], int n, bool vec)
-{
-    constexpr int W = 16 / (int)sizeof(T);
-    if (vec) {
-        struct alignas(16) V {
-            T x[W];
-        };
-#pragma unroll
-        for (int v = 0; v < R / W; ++v) {
-            if (v * W < n) {
-                V o;
-#pragma unroll
-                for (int k = 0; k < W; ++k)
-                    o.x[k] = col[v * W + k];
-                reinterpret_cast<V *>(qc)[v] = o;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (r < n)
-                qc[r] = col[r];
-    }
-}
-
-template <typename T>
-__device__ __forceinline__ bool q_vector_ok(const void *Q, int n)
-{
-    return ((n * (int)sizeof(T)) % 16) == 0 && ((reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
-}
 
 // Empty store for eigenvalues only.
 template <typename T, int NM>
@@ -1024,10 +1077,20 @@ __global__ void lane_kernel(KParams p)
             Q.setup(base, blockDim.x);
         }
         // every lane initialises its Q (dead and poisoned lanes too: the
-        // memory rows are read unconditionally during the passes)
+        // memory rows are read unconditionally during the passes).  Column s
+        // of the working Q is column phys(s) of the identity, or of the
+        // caller's basis with back_transform (Z P, P the permutation of the
+        // mirrored blocks).
+        const bool from_z = p.back && L.status == ST_RUN;
+        const T *zb = reinterpret_cast<const T *>(p.Q) + b * (long long)L.n * L.n;
+        const bool zvec = q_vector_ok<T>(p.Q, L.n);
 #pragma unroll
-        for (int s = 0; s < NM; ++s)
-            Q.init_col(s, (L.status == ST_RUN && s < L.n) ? L.phys(s) : s);
+        for (int s = 0; s < NM; ++s) {
+            if (from_z && s < L.n)
+                Q.init_col_from(s, zb + (long long)L.phys(s) * L.n, L.n, zvec);
+            else
+                Q.init_col(s, (L.status == ST_RUN && s < L.n) ? L.phys(s) : s);
+        }
     }
 
     if (SCHED == SCHED_FLAT) {

@@ -258,7 +258,13 @@ __global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams 
                 const int a = block_lo(zmask, s), bb = block_hi(zmask, s);
                 row = ((revmask >> a) & 1u) ? (a + bb - s) : s;
             }
-            A.Q.init_col(s, row);
+            // column `row` of the identity, or of the caller's basis with
+            // back_transform
+            if (p.back && status0 == ST_RUN && s < n)
+                A.Q.init_col_from(s, reinterpret_cast<const float *>(p.Q) + b * (long long)n * n + (long long)row * n,
+                                  n, q_vector_ok<float>(p.Q, n));
+            else
+                A.Q.init_col(s, row);
         }
         int parity = 0;
         for (;;) {

@@ -167,3 +167,93 @@ def test_unaligned_q_matches_aligned(dt, n, params):
     np.testing.assert_array_equal(lam.cpu().numpy(), ref[0])
     np.testing.assert_array_equal(Qo.cpu().numpy(), ref[1])
     np.testing.assert_array_equal(info.cpu().numpy(), ref[2])
+
+
+@pytest.mark.parametrize("dt,n,params", [(np.float32, 16, {}), (np.float32, 16, {"qstore": 4}),
+                                         (np.float32, 12, {}), (np.float32, 5, {}), (np.float32, 8, {}),
+                                         (np.float32, 32, {}), (np.float32, 16, {"kernel": 2}),
+                                         (np.float32, 16, {"qstore": 3}), (np.float64, 12, {}),
+                                         (np.float64, 7, {}), (np.float64, 8, {"kernel": 1}),
+                                         (np.float64, 32, {})])
+def test_back_transform_matches_oracle(dt, n, params):
+    """back_transform (BatchLAS page "algo_steqr", eigenvector accumulation):
+    the rotations are right-applied to the caller's basis Z.  With Z
+    orthogonal, V = Z Q must hold the eigenvectors of A = Z T Z^T within the
+    stated bounds, agree with the oracle run on the same Z (columns up to
+    sign), and leave the eigenvalues and info as without Z."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    from tests import helpers as H
+    batch = 1500
+    d, e = inputs.normal_problems(n, batch, dt, seed=40 + n)
+    Z = inputs.orthogonal_bases(n, batch, dt, seed=n)
+    ref = oracle_ref(d, e, True)
+    import oracle
+    oz = oracle.steqr(d, e, jobz=True, Z=Z)
+    dev = torch.device("cuda:0")
+    dg = torch.from_numpy(d.copy()).to(dev)
+    eg = torch.from_numpy(e.copy()).to(dev)
+    lam, V, info = bstq.solve(dg, eg, jobz=True, Z=torch.from_numpy(Z).to(dev), **params)
+    torch.cuda.synchronize()
+    lam, V, info = lam.cpu().numpy(), V.cpu().numpy(), info.cpu().numpy()
+    plain = run_gpu(d, e, **params)
+    np.testing.assert_array_equal(lam, plain[0])
+    np.testing.assert_array_equal(info, oz.info)
+    eps = H.eps_of(dt)
+    tn = H.norm1(d, e).astype(np.float64)
+    assert np.all(np.abs(lam.astype(np.float64) - ref.lam).max(1) <= H.lam_tol(n, dt, tn))
+    res, orth = H.back_residual_orth(d, e, Z, lam, V)
+    assert np.all(res <= 64 * n * eps * tn)
+    assert np.all(orth <= 64 * n * eps)
+    # V against Z times the GPU's own eigenvectors (same rotations, rows of Z
+    # rotated independently): within rounding
+    zq = Z.astype(np.float64) @ plain[1].astype(np.float64)
+    assert np.abs(zq - V).max() <= 64 * n * eps
+    # against the oracle's back-transformed vectors, column by column up to
+    # sign where the eigenvalue is well separated
+    lam64 = ref.lam.astype(np.float64)
+    gaps = np.minimum(np.abs(np.diff(lam64, axis=1, prepend=-np.inf)),
+                      np.abs(np.diff(lam64, axis=1, append=np.inf)))
+    ok = gaps > 1e-2 * tn[:, None]
+    sgn = np.sign((V.astype(np.float64) * oz.Q.astype(np.float64)).sum(1))
+    diff = np.abs(V.astype(np.float64) * sgn[:, None, :] - oz.Q.astype(np.float64)).max(1)
+    bound = 64 * n * eps * tn[:, None] / np.maximum(gaps, 1e-300)
+    assert np.all(diff[ok] <= np.maximum(bound[ok], 64 * n * eps))
+
+
+def test_back_transform_identity_basis_equals_plain():
+    """Z = I gives the plain eigenvectors exactly."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    d, e = inputs.normal_problems(16, 800, np.float32, seed=44)
+    plain = run_gpu(d, e)
+    dev = torch.device("cuda:0")
+    I = torch.eye(16, dtype=torch.float32, device=dev).expand(800, 16, 16)
+    lam, V, info = bstq.solve(torch.from_numpy(d.copy()).to(dev), torch.from_numpy(e.copy()).to(dev),
+                              jobz=True, Z=I)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(V.cpu().numpy(), plain[1])
+    np.testing.assert_array_equal(lam.cpu().numpy(), plain[0])
+
+
+def test_host_entry_point_back_transform():
+    """bstq_solve_host copies the basis in when back_transform is set."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    n, batch = 16, 1200
+    d, e = inputs.normal_problems(n, batch, np.float32, seed=45)
+    Z = inputs.orthogonal_bases(n, batch, np.float32, seed=3)
+    hd = torch.from_numpy(d.copy()).pin_memory()
+    he = torch.from_numpy(e.copy()).pin_memory()
+    hq = torch.from_numpy(np.ascontiguousarray(Z.transpose(0, 2, 1))).pin_memory()  # storage [b][j][i] = Z_ij
+    hi = torch.empty(batch, dtype=torch.int32).pin_memory()
+    dev = torch.empty(bstq.host_work_size(np.float32, True, n, batch, back_transform=True), dtype=torch.uint8,
+                      device="cuda")
+    bstq.solve_host(hd, he, hq, hi, dev, jobz=True, back_transform=True)
+    torch.cuda.synchronize()
+    lam, V, info = bstq.solve(torch.from_numpy(d.copy()).cuda(), torch.from_numpy(e.copy()).cuda(), jobz=True,
+                              Z=torch.from_numpy(Z).cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(hd.numpy(), lam.cpu().numpy())
+    np.testing.assert_array_equal(hq.numpy().transpose(0, 2, 1), V.cpu().numpy())
+    np.testing.assert_array_equal(hi.numpy(), info.cpu().numpy())
