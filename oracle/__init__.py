@@ -53,7 +53,7 @@ def _bind(lib):
         fn.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                       ctypes.c_int]
+                       ctypes.c_int, ctypes.c_int]
     lib.oracle_constant.restype = ctypes.c_double
     lib.oracle_constant.argtypes = [ctypes.c_int, ctypes.c_int]
     return lib
@@ -95,14 +95,19 @@ class Result:
 
 
 def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
-          sort: bool = True, nthreads: int = 1, lib=None, Z=None) -> Result:
+          sort: bool = True, nthreads: int = 1, lib=None, Z=None, scheme: str = "exp") -> Result:
     """Run the oracle on host arrays ``d`` (batch, n) and ``e`` (batch, n-1).
 
     The dtype of ``d`` (float32 or float64) selects the precision; ``e`` is
     cast to it.  With ``Z`` (batch, n, n) given (and jobz), the rotations are
     right-applied to Z instead of the identity (back_transform, BatchLAS page
     "algo_steqr", eigenvector accumulation): ``Q`` is then Z times the
-    eigenvectors.  Inputs are not modified."""
+    eigenvectors.  ``scheme`` selects the implicit step's update: "exp"
+    (each local similarity written out, the default) or "pg" (the scalars
+    (g, p, c, s) propagated across the sweep), page "algo_steqr", update
+    schemes.  Inputs are not modified."""
+    if scheme not in ("exp", "pg"):
+        raise ValueError("oracle: scheme must be 'exp' or 'pg'")
     d = np.asarray(d)
     if d.dtype not in (np.float32, np.float64):
         raise TypeError("oracle: d must be float32 or float64")
@@ -126,7 +131,7 @@ def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
     rc = fn(int(n), int(batch), mode, int(maxit_per_n), int(bool(sort)),
             lam.ctypes.data, ec.ctypes.data if ec.size else None,
             Qc.ctypes.data if jobz else None, info.ctypes.data, cnt.ctypes.data,
-            int(nthreads))
+            int(nthreads), 0 if scheme == "exp" else 1)
     if rc != 0:
         raise ValueError(f"oracle: invalid arguments (n={n}, batch={batch})")
     Q = None

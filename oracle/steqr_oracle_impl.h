@@ -97,7 +97,7 @@ static int FN(eidx)(FN(view_t) v, int p)
  * rotations, 2x2 direct solves).  Returns info: 0 converged, k > 0 the sweep
  * budget ran out with k off-diagonals still nonzero, -1 non-finite input.
  */
-static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort,
+static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort, int scheme,
                          real_t *d, const real_t *e_in, real_t *Q,
                          real_t *e, long *cnt)
 {
@@ -246,6 +246,37 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort,
             real_t r = FN(hyp1)(g);
             real_t mu = d1 - e1 / (g + R_COPYSIGN(r, g));
 
+            if (scheme == 1) {
+                /* algo_steqr, update schemes: PG propagates (g, p, c, s)
+                 * across the sweep.  The page gives the QR form; this is the
+                 * mirrored recurrence with the sweep reversed (QL form, in
+                 * converging coordinates), seeded with g = d_m - mu,
+                 * c = s = 1, p = 0:
+                 *   f = s e, b = c e, (c, s, r) = lartg(g, f), e_prev <- r,
+                 *   g* = d_i0 - p, r* = (d_i1 - g*) s + 2 c b, p = s r*,
+                 *   d_i0 <- g* + p, g = c r* - b;
+                 * after the last step d_lo <- d_lo - p and e_lo <- g. */
+                real_t g = DD(m) - mu, sp = 1, cp = 1, p = 0;
+                for (int q = 0; q < m - lo; ++q) {
+                    int i0 = m - q, i1 = m - q - 1;
+                    real_t f = sp * EE(i1), b = cp * EE(i1), rr;
+                    FN(lartg)(g, f, &cp, &sp, &rr);
+                    if (q > 0)
+                        EE(i0) = rr;
+                    real_t gs = DD(i0) - p;
+                    real_t rs = (DD(i1) - gs) * sp + (real_t)2 * cp * b;
+                    p = sp * rs;
+                    DD(i0) = gs + p;
+                    g = cp * rs - b;
+                    if (jobz)
+                        FN(rot_cols)(n, Q, QC(i0), QC(i1), cp, sp);
+                    cnt[1] += 1;
+                }
+                DD(lo) = DD(lo) - p;
+                EE(lo) = g;
+                continue;
+            }
+
             /* algo_steqr, implicit bulge chase: the first rotation comes from
              * the shifted corner (d_m - mu, e_{m-1}) at the far end of the
              * sweep, every later one from (e_current, bulge).  Each step is
@@ -341,7 +372,7 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort,
 
 /* Batch driver arguments, one worker per contiguous slice of the batch. */
 typedef struct {
-    int n, jobz, maxit_per_n, sort;
+    int n, jobz, maxit_per_n, sort, scheme;
     long b0, b1;
     real_t *d;
     const real_t *e;
@@ -359,7 +390,7 @@ static void *FN(worker)(void *arg)
         real_t *db = jb->d + b * n;
         const real_t *eb = jb->e + b * (n > 1 ? n - 1 : 0);
         real_t *Qb = jb->jobz ? jb->Q + b * (long)n * n : (real_t *)0;
-        jb->info[b] = FN(steqr_one)(n, jb->jobz, jb->maxit_per_n, jb->sort,
+        jb->info[b] = FN(steqr_one)(n, jb->jobz, jb->maxit_per_n, jb->sort, jb->scheme,
                                     db, eb, Qb, ework, jb->cnt);
     }
     return (void *)0;
@@ -367,13 +398,14 @@ static void *FN(worker)(void *arg)
 
 /* Solve a batch of problems (d: batch x n, e: batch x (n-1), Q: batch x n x n
  * column-major per problem) on nthreads host threads, static partition.
+ * scheme: 0 the EXP update, 1 the PG update (algo_steqr, update schemes).
  * counters[0..2] receive the summed (implicit steps, rotations, 2x2 solves).
  * Returns 0, or -1 for invalid arguments. */
 int FN(oracle_steqr_batch)(int n, long batch, int jobz, int maxit_per_n,
                            int sort, real_t *d, const real_t *e, real_t *Q,
-                           int *info, long *counters, int nthreads)
+                           int *info, long *counters, int nthreads, int scheme)
 {
-    if (n < 1 || n > 64 || batch < 0 || maxit_per_n < 0)
+    if (n < 1 || n > 64 || batch < 0 || maxit_per_n < 0 || scheme < 0 || scheme > 1)
         return -1;
     if (nthreads < 1)
         nthreads = 1;
@@ -388,6 +420,7 @@ int FN(oracle_steqr_batch)(int n, long batch, int jobz, int maxit_per_n,
         jobs[t].jobz = jobz;
         jobs[t].maxit_per_n = maxit_per_n;
         jobs[t].sort = sort;
+        jobs[t].scheme = scheme;
         jobs[t].b0 = batch * t / nthreads;
         jobs[t].b1 = batch * (t + 1) / nthreads;
         jobs[t].d = d;

@@ -41,6 +41,11 @@ MUTATIONS = [
     ("block_ignores_exact_zero", "while (le < n - 1 && e[le] != (real_t)0)",
      "while (le < n - 1 && e[le] != (real_t)-12345)"),
     ("back_transform_ignored", "    if (jobz == 1)\n", "    if (jobz >= 1)\n"),
+    ("pg_dropped_2cb", "real_t rs = (DD(i1) - gs) * sp + (real_t)2 * cp * b;",
+     "real_t rs = (DD(i1) - gs) * sp + cp * b;"),
+    ("pg_missing_fixup", "DD(lo) = DD(lo) - p;", "DD(lo) = DD(lo);"),
+    ("pg_bulge_unscaled", "real_t f = sp * EE(i1), b = cp * EE(i1), rr;",
+     "real_t f = EE(i1), b = cp * EE(i1), rr;"),
 ]
 
 
@@ -110,6 +115,20 @@ def pin_failures(lib):
         rel = np.abs((r.lam.astype(np.float64) - ref) / ref).max(1)
         check("graded_rate", r.sweeps <= 1.5 * 16 * 100)
         check("graded_relacc", np.median(rel) <= 100 * eps)
+        # PG update scheme: same spectrum and eigenpair bounds as EXP
+        for n in (5, 12):
+            d, e = inputs.normal_problems(n, 40, dt, seed=50 + n)
+            r = oracle.steqr(d, e, jobz=True, lib=lib, scheme="pg")
+            tn = H.norm1(d, e).astype(np.float64)
+            ref = np.linalg.eigvalsh(H.dense(d, e))
+            check(f"pg_info{n}", np.all(r.info == 0))
+            lam = np.nan_to_num(r.lam.astype(np.float64), nan=1e300)
+            check(f"pg_eigvalsh{n}", np.all(np.abs(lam - ref).max(1) <= H.lam_tol(n, dt, tn)))
+            if np.all(np.isfinite(r.Q)):
+                res, orth = H.residual_orth(d, e, r.lam, r.Q)
+                check(f"pg_res{n}", np.all(res <= 64 * n * eps * tn))
+            else:
+                bad.append(f"pg_finite{n}")
         # back_transform: the rotations are right-applied to an orthogonal Z,
         # so Z Q holds the eigenvectors of Z T Z^T
         d, e = inputs.normal_problems(7, 20, dt, seed=6)

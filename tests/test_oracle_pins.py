@@ -419,3 +419,48 @@ def test_back_transform_solves_the_dense_problem(dt, n):
     np.testing.assert_array_equal(r.lam, plain.lam)
     zq = Z.astype(np.float64) @ plain.Q.astype(np.float64)
     assert np.abs(zq - r.Q).max() <= 64 * n * eps
+
+
+# --- PG update scheme (BatchLAS page "algo_steqr", update schemes: PG
+# propagates (g, p, c, s) across the sweep; EXP writes each local similarity;
+# both perform the same implicit step) ---
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+@pytest.mark.parametrize("n", [2, 3, 6, 12, 17, 32])
+def test_pg_scheme_solves_like_exp(dt, n):
+    batch = 300
+    d, e = inputs.normal_problems(n, batch, dt, seed=60 + n)
+    eps = H.eps_of(dt)
+    tn = H.norm1(d, e).astype(np.float64)
+    pg = oracle.steqr(d, e, jobz=True, scheme="pg")
+    ex = oracle.steqr(d, e, jobz=True, scheme="exp")
+    assert np.all(pg.info == 0)
+    ref = np.linalg.eigvalsh(H.dense(d, e))
+    assert np.all(np.abs(pg.lam.astype(np.float64) - ref).max(1) <= H.lam_tol(n, dt, tn))
+    res, orth = H.residual_orth(d, e, pg.lam, pg.Q)
+    assert np.all(res <= 64 * n * eps * tn)
+    assert np.all(orth <= 64 * n * eps)
+    # the same implicit steps: sweep and rotation counts within 2 %
+    assert abs(pg.sweeps - ex.sweeps) <= 0.02 * ex.sweeps + 2
+    assert abs(pg.rotations - ex.rotations) <= 0.02 * ex.rotations + 2
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_pg_scheme_toeplitz_and_hard_cases(dt):
+    n = 16
+    rng = np.random.default_rng(7)
+    a, b = rng.standard_normal(2)
+    d = np.full((1, n), a, dtype=dt)
+    e = np.full((1, n - 1), b, dtype=dt)
+    r = oracle.steqr(d, e, jobz=False, scheme="pg")
+    k = np.arange(1, n + 1)
+    closed = np.sort(a + 2 * b * np.cos(k * np.pi / (n + 1)))
+    tn = H.norm1(d, e).astype(np.float64)
+    assert np.abs(r.lam[0].astype(np.float64) - closed).max() <= H.lam_tol(n, dt, tn)[0]
+    dm, em, _, _ = inputs.mixed_problems(32, 400, dt, seed=3)
+    pg = oracle.steqr(dm, em, jobz=False, scheme="pg")
+    ex = oracle.steqr(dm, em, jobz=False, scheme="exp")
+    np.testing.assert_array_equal(pg.info, ex.info)
+    tn = H.norm1(dm, em).astype(np.float64)
+    ok = np.isfinite(ex.lam).all(1)
+    assert np.all(np.abs(pg.lam[ok].astype(np.float64) - ex.lam[ok]).max(1) <= 2 * H.lam_tol(32, dt, tn[ok]))
