@@ -90,7 +90,18 @@ typedef struct {
                               it holds Z times the eigenvectors of T, sorted
                               with lambda (BatchLAS page "algo_steqr",
                               eigenvector accumulation: back_transform).     */
+    int update_scheme;     /* bstq_update_scheme: 0 (default) EXP, 1 PG.    */
 } bstq_params;
+
+/* Form of the implicit step (BatchLAS page "algo_steqr", update schemes).
+ * EXP writes each local similarity G^T T G out; PG propagates the scalars
+ * (g, p, c, s) across the sweep.  Both perform the same implicit step.  PG
+ * runs in the dynamic-position kernels: with kernel = AUTO it selects them,
+ * with kernel = STATIC it returns -10. */
+typedef enum {
+    BSTQ_UPDATE_EXP = 0,
+    BSTQ_UPDATE_PG = 1
+} bstq_update_scheme;
 
 /* Kernel family.  STATIC: d and e in registers, the chase unrolled over
  * compile-time positions (Q in registers, shared or global memory per

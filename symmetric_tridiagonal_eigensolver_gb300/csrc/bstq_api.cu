@@ -166,6 +166,8 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
             return -10;
         if (p->back_transform != 0 && p->back_transform != 1)
             return -10;
+        if (p->update_scheme != 0 && p->update_scheme != 1)
+            return -10;
         if (p->threads_per_block != 0 &&
             (p->threads_per_block < 32 || p->threads_per_block > 1024 || p->threads_per_block % 32))
             return -10;
@@ -186,7 +188,10 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
             nm = v;
             break;
         }
-    const int family = (p && p->kernel) ? p->kernel : default_family(dtype, jobz, nm);
+    const bool pg = p && p->update_scheme == 1;
+    const int family = (p && p->kernel) ? p->kernel : (pg ? FAMILY_DYNAMIC : default_family(dtype, jobz, nm));
+    if (pg && family != FAMILY_DYNAMIC)
+        return -10;  // the PG step runs in the dynamic-position kernels only
     const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
     int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm, sched)) : 0;
     if (family == FAMILY_DYNAMIC && jobz)
@@ -315,6 +320,7 @@ int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const voi
     kp.sort = (p && p->no_sort) ? 0 : 1;
     kp.ppb = pl.ppb;
     kp.back = (Q && p && p->back_transform) ? 1 : 0;
+    kp.scheme = (p && p->update_scheme) ? 1 : 0;
     (void)dtype;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
@@ -593,6 +599,7 @@ extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64
     kp.sort = q.no_sort ? 0 : 1;
     kp.ppb = pl.ppb;
     kp.back = q.back_transform ? 1 : 0;
+    kp.scheme = q.update_scheme ? 1 : 0;
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (err != cudaSuccess)

@@ -104,8 +104,10 @@ struct DynLane {
     T pre, sc, aeff, anorm;
     int jtot, budget;
     int task, m;
-    T f, g;        // running pair
+    T f, g;        // running pair (PG: f is the running g of the recurrence)
     T cs2, sn2;    // pending 2x2 rotation
+    bool pg;       // PG update scheme for sweeps (else EXP)
+    T pg_c, pg_s, pg_p;  // PG: previous rotation and p
     // pass state
     int L, C;      // steps of the current task, current position
     T a_reg, b_reg;  // d_C and e_{C-1} as updated by the previous step
@@ -362,6 +364,8 @@ struct DynLane {
         L = m - lo;  // 1 for a 2x2 task
         a_reg = D(C);
         b_reg = Ev(C - 1);
+        pg_c = pg_s = T(1);
+        pg_p = T(0);
         if constexpr (WANTZ)
             q.load(C, cur);
         if constexpr (FASTQ) {
@@ -375,6 +379,40 @@ struct DynLane {
     {
         const bool sweep = task == TASK_SWEEP;
         T cs, sn, r = T(0);
+        if (sweep && pg) {
+            // PG (page "algo_steqr", update schemes), QL form: the scalars
+            // (g, p, c, s) run across the sweep; d_C is final after this
+            // step, e_C takes r, and the last step closes d_lo and e_lo.
+            const T ev = Ev(C - 1);
+            const T fb = pg_s * ev, bb = pg_c * ev;
+            if constexpr (sizeof(T) == 8)
+                lartg_fast(f, fb, cs, sn, r);
+            else
+                lartg(f, fb, cs, sn, r);
+            if (k > 0)
+                setE(C, r);
+            const T gs = D(C) - pg_p;
+            const T rs = fma(D(C - 1) - gs, sn, T(2) * cs * bb);
+            pg_p = sn * rs;
+            setD(C, gs + pg_p);
+            f = fma(cs, rs, -bb);
+            pg_c = cs;
+            pg_s = sn;
+            if (C - 1 == lo) {
+                setD(lo, D(lo) - pg_p);
+                setE(lo, f);
+            }
+        } else {
+            step_exp(k, sweep, cs, sn, r);
+        }
+        step_q(cs, sn);
+        --C;
+    }
+
+    // EXP step (and the 2x2 solve of either scheme): the similarity written
+    // out on the pair (C, C-1).
+    __device__ __forceinline__ void step_exp(int k, bool sweep, T &cs, T &sn, T &r)
+    {
         if (sweep) {
             if constexpr (sizeof(T) == 8)
                 lartg_fast(f, g, cs, sn, r);
@@ -406,6 +444,11 @@ struct DynLane {
             setD(C - 1, dm);
             setE(C - 1, en);
         }
+    }
+
+    // Eigenvector update of the step's rotation on columns (C, C-1).
+    __device__ __forceinline__ void step_q(T cs, T sn)
+    {
         if constexpr (FASTQ) {
             // q_C = da x, q_{C-1} = db y.  Form 1 (|cs| >= |sn|):
             //   x' = x + P y, y' = y - M x, da' = cs da, db' = cs db;
@@ -463,7 +506,6 @@ struct DynLane {
                 q.store(C - 1, nx);
             }
         }
-        --C;
     }
 
     __device__ __forceinline__ void post_pass()
@@ -494,6 +536,7 @@ __global__ void dyn_kernel(KParams p)
     L.sdl = L.se + NM * tpb;
     L.sil = L.sdl + NM * tpb;
     L.da = L.ia = T(1);
+    L.pg = p.scheme == 1;
     if constexpr (WANTZ) {
         // Q scratch in global memory: per block NM columns x G vectors x tpb
         constexpr int G = DynQ<T, NM>::G;

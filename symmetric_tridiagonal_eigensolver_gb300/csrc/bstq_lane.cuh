@@ -53,6 +53,7 @@ struct KParams {
     int sort;          // 1: ascending output
     int ppb;           // problems per block (split-role kernel)
     int back;          // 1: Q holds the basis Z on entry (back_transform)
+    int scheme;        // 0 EXP, 1 PG update (dynamic-position kernels)
 };
 
 // ---------------------------------------------------------------------------

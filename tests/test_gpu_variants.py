@@ -257,3 +257,43 @@ def test_host_entry_point_back_transform():
     np.testing.assert_array_equal(hd.numpy(), lam.cpu().numpy())
     np.testing.assert_array_equal(hq.numpy().transpose(0, 2, 1), V.cpu().numpy())
     np.testing.assert_array_equal(hi.numpy(), info.cpu().numpy())
+
+
+@pytest.mark.parametrize("dt,n,jobz,batch", [(np.float64, 12, True, 4000), (np.float64, 12, False, 4000),
+                                             (np.float32, 16, True, 4000), (np.float64, 3, True, 3001),
+                                             (np.float64, 32, True, 2000), (np.float32, 27, False, 2500),
+                                             (np.float64, 12, True, 32768)])
+def test_pg_update_scheme_matches_oracle(dt, n, jobz, batch):
+    """PG update (page "algo_steqr", update schemes) against the oracle's PG
+    scheme on the same inputs: the benchmark spec's bounds, info exactly."""
+    d, e = inputs.normal_problems(n, batch, dt, seed=70 + n)
+    ref = oracle_ref(d, e, jobz, scheme="pg")
+    a = run_gpu(d, e, jobz=jobz, update_scheme=1)
+    check_parity(d, e, *a, ref, what=f"pg n={n}")
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_pg_update_scheme_hard_cases(dt):
+    d, e, _, _ = inputs.mixed_problems(32, 3000, dt, seed=9)
+    ref = oracle_ref(d, e, True, scheme="pg")
+    a = run_gpu(d, e, jobz=True, update_scheme=1)
+    check_parity(d, e, *a, ref, what="pg mixed")
+
+
+def test_pg_with_static_family_is_rejected():
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    with pytest.raises(bstq.BstqError) as ei:
+        run_gpu(*inputs.normal_problems(16, 64, np.float32, seed=1), update_scheme=1, kernel=1)
+    assert ei.value.code == -10
+
+
+def test_pg_and_exp_agree_on_the_gpu():
+    """The two update forms of the same implicit step: eigenvalues within the
+    bound of each other, same info."""
+    d, e = inputs.normal_problems(12, 5000, np.float64, seed=80)
+    a = run_gpu(d, e, update_scheme=1)
+    b = run_gpu(d, e, update_scheme=0, kernel=2)
+    np.testing.assert_array_equal(a[2], b[2])
+    from tests import helpers as H
+    tn = H.norm1(d, e).astype(np.float64)
+    assert np.all(np.abs(a[0] - b[0]).max(1) <= 2 * H.lam_tol(12, np.float64, tn))
