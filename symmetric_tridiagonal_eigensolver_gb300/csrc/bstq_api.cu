@@ -25,7 +25,7 @@ struct Plan {
     int ppb = 0;  // problems per block (split-role kernel)
 };
 
-constexpr int kNmList[] = {4, 8, 12, 16, 24, 32};
+constexpr int kNmList[] = {4, 8, 12, 16, 24, 32, 48, 64};
 
 thread_local char g_last_error[256] = "";
 
@@ -135,11 +135,13 @@ int default_sched(int, int) { return SCHED_FLAT; }
 //   double: dynamic at every n (n=4 V 0.111 vs 0.112 ms, n=8 V 0.44 vs
 //          0.53 ms, n=12 V 0.98 vs 1.31 ms, n=12 N 0.49 vs 0.51 ms):
 //          FP64-bound, and the dynamic kernel has no union of position
-//          ranges and a factored Q update.
+//          ranges and a factored Q update;
+//   n > 32: dynamic (the static family is built up to n = 32).
 int default_family(int dtype, int jobz, int nm)
 {
     (void)jobz;
-    (void)nm;
+    if (nm > 32)
+        return FAMILY_DYNAMIC;  // the only family built above n = 32
     return dtype == 0 ? FAMILY_STATIC : FAMILY_DYNAMIC;
 }
 
@@ -484,7 +486,7 @@ extern "C" const char *bstq_status_string(int code)
     case BSTQ_ERR_NODEVICE: return "no usable CUDA device is current";
     case -1: return "invalid dtype";
     case -2: return "invalid jobz";
-    case -3: return "n outside [1, 32]";
+    case -3: return "n outside [1, 64]";
     case -4: return "invalid batch";
     case -5: return "d is NULL or misaligned";
     case -6: return "e is NULL or misaligned";

@@ -16,6 +16,8 @@
 // schedulers of "perf_steqr", section "Lockstep flat solver".
 #pragma once
 
+#include <type_traits>
+
 #include "bstq_lane.cuh"
 
 namespace bstq {
@@ -52,6 +54,7 @@ struct DynQ {
         for (int g = 0; g < G; ++g)
             base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
     }
+    __device__ __forceinline__ V16 &vec(int k, int g) const { return base[(k * G + g) * stride]; }
     // Column s from the caller's basis: rows 0 .. n-1 of zc, zero below
     // (back_transform).
     __device__ __forceinline__ void init_col_from(int s, const T *zc, int n, bool vec) const
@@ -91,13 +94,22 @@ struct DynLane {
     using E = typename Q_::E;
     static constexpr int NE = Q_::NE;
     static constexpr bool FASTQ = dyn_fastq<T, WANTZ>();
+    // Block-boundary and mirror masks: one bit per entry.
+    using Mask = typename std::conditional<(NM > 32), unsigned long long, unsigned>::type;
+    static constexpr int MASK_BITS = 8 * (int)sizeof(Mask);
+    // The column shared by successive rotations of a sweep stays in
+    // registers.  For double above n = 32 the whole next column would not
+    // fit beside it, so that column is read and rotated in groups of vectors
+    // (step_q_carry_chunked); float reads the whole next column at once
+    // (up to 32 packed pairs), which measured faster.
+    static constexpr bool CHUNKED = sizeof(T) == 8 && NM > 32;
 
     T *sd, *se;  // this lane's d and e in shared memory
     T *sdl, *sil;  // column scales delta_j and 1/delta_j (FASTQ)
     int ms;      // their stride (blockDim.x)
     T da, ia;    // scale and inverse scale of the carried column C (FASTQ)
     int n, status, info;
-    unsigned zmask, revmask;
+    Mask zmask, revmask;
     bool inblock;
     int bnext, lb, le, lo;
     int iscale;
@@ -122,7 +134,7 @@ struct DynLane {
     __device__ __forceinline__ int phys(int s) const
     {
         int a = block_lo(zmask, s), b = block_hi(zmask, s);
-        return ((revmask >> a) & 1u) ? (a + b - s) : s;
+        return ((revmask >> a) & 1) ? (a + b - s) : s;
     }
 
     __device__ __forceinline__ void scale_factors(T an, int &isc, T &pr, T &s, T &ae) const
@@ -172,7 +184,7 @@ struct DynLane {
         C = 0;
         if (!live) {
             status = ST_DEAD;
-            zmask = ~0u;
+            zmask = ~Mask(0);
             return;
         }
         const T *dg = reinterpret_cast<const T *>(p.d) + b * n;
@@ -186,9 +198,9 @@ struct DynLane {
             setE(i, ei);
             bad |= !isfinite(di) || !isfinite(ei);
             if (i >= n - 1 || ei == T(0))
-                zmask |= 1u << i;
+                zmask |= Mask(1) << i;
         }
-        zmask |= n < 32 ? (~0u << n) : 0u;
+        zmask |= n < MASK_BITS ? (~Mask(0) << n) : Mask(0);
         status = bad ? ST_BAD : ST_RUN;
         if (bad)
             return;
@@ -206,7 +218,7 @@ struct DynLane {
                         y = (y * pr) * s;
                     }
                     if (dabs(x) > dabs(y))
-                        revmask |= 1u << a;
+                        revmask |= Mask(1) << a;
                 }
             }
             a = z + 1;
@@ -215,7 +227,7 @@ struct DynLane {
             for (int s = 0; s < n; ++s) {
                 const int ps = phys(s);
                 setD(s, dg[ps]);
-                if (s < n - 1 && !((zmask >> s) & 1u)) {
+                if (s < n - 1 && !((zmask >> s) & 1)) {
                     const int pn = phys(s + 1);
                     setE(s, eg[ps < pn ? ps : pn]);
                 }
@@ -449,6 +461,98 @@ struct DynLane {
     // Eigenvector update of the step's rotation on columns (C, C-1).
     __device__ __forceinline__ void step_q(T cs, T sn)
     {
+        if constexpr (!WANTZ)
+            return;  // eigenvalues only: no Q (q.base is not set)
+        else if constexpr (CHUNKED)
+            step_q_carry_chunked(cs, sn);
+        else
+            step_q_carry(cs, sn);
+    }
+
+    // step_q_carry for double above n = 32: column C-1 is read four 16-byte
+    // vectors at a time, the next group's reads issued before this group's
+    // writes, so only the carried column and two groups are live in
+    // registers.
+    __device__ __forceinline__ void step_q_carry_chunked(T cs, T sn)
+    {
+        constexpr int G = Q_::G;
+        constexpr int K = 4;  // vectors per group
+        static_assert(G % K == 0, "column vectors in whole groups");
+        using V = typename Q_::V16;
+        T c1, c2, da2 = T(0), db2 = T(0), ia2 = T(0), ib2 = T(0);
+        bool f1 = true;
+        typename El<T>::R rr;
+        if constexpr (FASTQ) {
+            const T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
+            f1 = (__double_as_longlong(cs) & 0x7fffffffffffffffll) >=
+                 (__double_as_longlong(sn) & 0x7fffffffffffffffll);
+            const T rp = rcp_nr(f1 ? cs : sn);
+            const T t = (f1 ? sn : cs) * rp;
+            const T P = t * (db * ia), M = t * (da * ib);
+            c1 = f1 ? P : M;
+            c2 = f1 ? -M : -P;
+            da2 = (f1 ? cs : sn) * (f1 ? da : db);
+            db2 = (f1 ? cs : -sn) * (f1 ? db : da);
+            ia2 = (f1 ? ia : ib) * rp;
+            ib2 = (f1 ? ib : -ia) * rp;
+        } else {
+            rr = El<T>::make(cs, sn);
+        }
+        V nx[2][K];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            nx[0][k] = q.vec(C - 1, k);
+#pragma unroll
+        for (int grp = 0; grp < G / K; ++grp) {
+            const int bsel = grp & 1;
+            if (grp + 1 < G / K) {
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+                    nx[bsel ^ 1][k] = q.vec(C - 1, (grp + 1) * K + k);
+            }
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int j = 2 * (grp * K + k);
+                E u0 = cur[j], u1 = cur[j + 1];
+                E v0 = nx[bsel][k].a, v1 = nx[bsel][k].b;
+                if constexpr (FASTQ) {
+                    const E s10 = f1 ? v0 : u0, s20 = f1 ? u0 : v0;
+                    const E s11 = f1 ? v1 : u1, s21 = f1 ? u1 : v1;
+                    u0 = fma(c1, s10, s20);
+                    v0 = fma(c2, s20, s10);
+                    u1 = fma(c1, s11, s21);
+                    v1 = fma(c2, s21, s11);
+                } else {
+                    El<T>::rot(u0, v0, rr);
+                    El<T>::rot(u1, v1, rr);
+                }
+                q.vec(C, grp * K + k) = V{u0, u1};
+                cur[j] = v0;
+                cur[j + 1] = v1;
+            }
+        }
+        if constexpr (FASTQ) {
+            sdl[C * ms] = da2;
+            sil[C * ms] = ia2;
+            da = db2;
+            ia = ib2;
+        }
+        if (C - 1 == lo) {
+            // end of the sweep: the carried column is final
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                q.vec(C - 1, g) = V{cur[2 * g], cur[2 * g + 1]};
+            if constexpr (FASTQ) {
+                sdl[(C - 1) * ms] = db2;
+                sil[(C - 1) * ms] = ib2;
+            }
+        }
+    }
+
+    // Column C is in registers (cur), column C-1 is read, and C-1 becomes
+    // the carried column.
+    __device__ __forceinline__ void step_q_carry(T cs, T sn)
+    {
         if constexpr (FASTQ) {
             // q_C = da x, q_{C-1} = db y.  Form 1 (|cs| >= |sn|):
             //   x' = x + P y, y' = y - M x, da' = cs da, db' = cs db;
@@ -607,10 +711,61 @@ __global__ void dyn_kernel(KParams p)
         p.info[b] = -1;
         return;
     }
+    const bool sorted = p.sort && L.status == ST_DONE;
+    if constexpr (NM > 32) {
+        // n > 32: rolled ranking and column copy, 16 bytes at a time, so no
+        // per-entry arrays live in registers
+        using Q_ = DynQ<T, NM>;
+        constexpr int W = 16 / (int)sizeof(T);
+        const bool vec = WANTZ && q_vector_ok<T>(p.Q, n);
+        for (int s = 0; s < n; ++s) {
+            const T ds = L.D(s);
+            const int phs = L.phys(s);
+            int pos = phs;
+            if (sorted) {
+                pos = 0;
+                for (int t = 0; t < n; ++t) {
+                    const T dt = L.D(t);
+                    pos += (dt < ds || (dt == ds && L.phys(t) < phs)) ? 1 : 0;
+                }
+            }
+            dout[pos] = ds;
+            if constexpr (WANTZ) {
+                T scale = T(1);
+                if constexpr (LaneT::FASTQ)
+                    scale = L.sdl[s * tpb];  // Q = Qt diag(delta)
+                T *qc = qout + (long long)pos * n;
+                for (int g = 0; g < Q_::G && g * W < n; ++g) {
+                    const typename Q_::V16 v = L.q.vec(s, g);
+                    T x[W];
+                    El<T>::get(v.a, &x[0]);
+                    El<T>::get(v.b, &x[Q_::RPE]);
+#pragma unroll
+                    for (int k = 0; k < W; ++k)
+                        x[k] = LaneT::FASTQ ? x[k] * scale : x[k];
+                    if (vec) {
+                        struct alignas(16) V {
+                            T y[W];
+                        } o;
+#pragma unroll
+                        for (int k = 0; k < W; ++k)
+                            o.y[k] = x[k];
+                        reinterpret_cast<V *>(qc)[g] = o;
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < W; ++k)
+                            if (g * W + k < n)
+                                qc[g * W + k] = x[k];
+                    }
+                }
+            }
+        }
+        p.info[b] = (L.status == ST_FAIL) ? L.info : 0;
+        return;
+    }
     // eigenvalues into registers for the ranking
     T dv[NM];
     int ph[NM], pos[NM];
-    const bool sorted = p.sort && L.status == ST_DONE;
 #pragma unroll
     for (int s = 0; s < NM; ++s) {
         dv[s] = s < n ? L.D(s) : T(0);

@@ -377,6 +377,16 @@ __device__ __forceinline__ int block_hi(unsigned zmask, int s)
 {
     return s + __ffs(zmask >> s) - 1;
 }
+// 64-bit forms for problems with more than 32 entries (dynamic kernels).
+__device__ __forceinline__ int block_lo(unsigned long long zmask, int s)
+{
+    unsigned long long below = s > 0 ? (zmask & ((1ull << s) - 1ull)) : 0ull;
+    return below ? (64 - __clzll((long long)below)) : 0;
+}
+__device__ __forceinline__ int block_hi(unsigned long long zmask, int s)
+{
+    return s + __ffsll((long long)(zmask >> s)) - 1;
+}
 
 // ---------------------------------------------------------------------------
 // Pass entry.  A pass is left only at group boundaries (after positions

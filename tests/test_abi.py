@@ -48,7 +48,7 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     assert solve(7, 1, 8, 10, good, good, good, good, None) == -1
     assert solve(0, 5, 8, 10, good, good, good, good, None) == -2
     assert solve(0, 1, 0, 10, good, good, good, good, None) == -3
-    assert solve(0, 1, 33, 10, good, good, good, good, None) == -3
+    assert solve(0, 1, bstq.MAX_N + 1, 10, good, good, good, good, None) == -3
     assert solve(0, 1, 8, -1, good, good, good, good, None) == -4
     assert solve(0, 1, 8, 0, None, None, None, None, None) == 0   # batch 0: no-op
     assert solve(0, 1, 8, 10, None, good, good, good, None) == -5

@@ -159,3 +159,59 @@ def test_unsorted_output_order(dt):
     same = np.abs(lam - ref.lam).max(1) <= tol
     assert same.mean() >= 0.9, same.mean()
     assert not np.all(np.diff(lam, axis=1) >= 0)   # really left unsorted
+
+
+# --- n > 32 (the n <= 32 cliff removed: the dynamic-position kernels at
+# compile-time maxima 48 and 64) ---
+
+@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("jobz", [True, False])
+@pytest.mark.parametrize("n", [33, 40, 48, 49, 57, 64])
+def test_beyond_32(dt, n, jobz):
+    _case(dt, n, 2000 + 3 * n, jobz=jobz, seed=200 + n)
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_mixed_hard_cases_n64(dt):
+    n, batch = 64, 4000
+    d, e, labels, ab = inputs.mixed_problems(n, batch, dt, seed=1)
+    ref = oracle_ref(d, e, jobz=True)
+    lam, Q, info = run_gpu(d, e, jobz=True)
+    check_parity(d, e, lam, Q, info, ref, what=f"mixed n=64 {np.dtype(dt).name}")
+    z = labels == inputs.CLASS_INDEX["zero"]
+    assert np.all(lam[z] == 0)
+    assert np.all(Q[z] == np.eye(n, dtype=dt))
+    tp = np.nonzero(labels == inputs.CLASS_INDEX["toeplitz"])[0]
+    tn = H.norm1(d, e).astype(np.float64)
+    for b in tp[:100]:
+        cf = H.toeplitz_eigenvalues(n, d[b, 0], e[b, 0]).astype(np.float64)
+        assert np.max(np.abs(lam[b] - cf)) <= H.lam_tol(n, dt, tn[b])
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_beyond_32_variants(dt):
+    """n = 64: nested = flat, PG within bounds, back_transform, unaligned Q."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    n, batch = 64, 1500
+    d, e = inputs.normal_problems(n, batch, dt, seed=300)
+    a = run_gpu(d, e)
+    b = run_gpu(d, e, scheduler=2)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    check_parity(d, e, *run_gpu(d, e, update_scheme=1), oracle_ref(d, e, True, scheme="pg"), what="pg n=64")
+    Z = inputs.orthogonal_bases(n, batch, dt, seed=5)
+    dev = torch.device("cuda:0")
+    lam, V, info = bstq.solve(torch.from_numpy(d.copy()).to(dev), torch.from_numpy(e.copy()).to(dev), jobz=True,
+                              Z=torch.from_numpy(Z).to(dev))
+    torch.cuda.synchronize()
+    res, orth = H.back_residual_orth(d, e, Z, lam.cpu().numpy(), V.cpu().numpy())
+    tn = H.norm1(d, e).astype(np.float64)
+    eps = H.eps_of(dt)
+    assert np.all(res <= 64 * n * eps * tn) and np.all(orth <= 64 * n * eps)
+    buf = torch.full((batch * n * n + 1,), float("nan"), dtype=lam.dtype, device=dev)
+    Qu = buf[1:].view(batch, n, n)
+    lam2, Q2, info2 = bstq.solve(torch.from_numpy(d.copy()).to(dev), torch.from_numpy(e.copy()).to(dev), jobz=True,
+                                 Q=Qu)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(Q2.cpu().numpy(), a[1])
