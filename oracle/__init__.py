@@ -54,6 +54,12 @@ def _bind(lib):
                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_int, ctypes.c_int]
+    for suffix in ("f32", "f64"):
+        fn = getattr(lib, f"oracle_syev_batch_{suffix}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     lib.oracle_constant.restype = ctypes.c_double
     lib.oracle_constant.argtypes = [ctypes.c_int, ctypes.c_int]
     return lib
@@ -139,3 +145,38 @@ def steqr(d, e, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
         # stored column-major per problem: memory [b][j][i] = Q_ij
         Q = np.ascontiguousarray(np.swapaxes(Qc, 1, 2))
     return Result(lam, Q, info, int(cnt[0]), int(cnt[1]), int(cnt[2]))
+
+
+def syev(A, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N, sort: bool = True,
+         nthreads: int = 1, lib=None, scheme: str = "exp") -> Result:
+    """Fused small-n dense symmetric eigensolver on host arrays: ``A``
+    (batch, n, n), of which the lower triangle (A[b, i, j], i >= j) is read.
+    Householder reduction to tridiagonal form, then the steqr solve with the
+    reduction's Q as the basis (back_transform).  Returns a Result with
+    ``lam`` (batch, n), ``Q`` (batch, n, n) the eigenvectors of A (None when
+    jobz = N), ``info`` and the steqr counters.  Inputs are not modified."""
+    A = np.asarray(A)
+    if A.dtype not in (np.float32, np.float64):
+        raise TypeError("oracle: A must be float32 or float64")
+    if scheme not in ("exp", "pg"):
+        raise ValueError("oracle: scheme must be 'exp' or 'pg'")
+    dt = A.dtype
+    if A.ndim == 2:
+        A = A[None]
+    batch, n, n2 = A.shape
+    if n != n2:
+        raise ValueError("oracle: A must be (batch, n, n)")
+    Ac = np.ascontiguousarray(np.swapaxes(A, 1, 2))  # memory [b][j][i] = A_ij
+    W = np.empty((batch, n), dtype=dt)
+    Vc = np.empty((batch, n, n), dtype=dt) if jobz else None
+    info = np.zeros(batch, dtype=np.int32)
+    cnt = np.zeros(3, dtype=np.int64)
+    lib = lib if lib is not None else _load()
+    fn = lib.oracle_syev_batch_f32 if dt == np.float32 else lib.oracle_syev_batch_f64
+    rc = fn(int(n), int(batch), int(bool(jobz)), int(maxit_per_n), int(bool(sort)),
+            Ac.ctypes.data, W.ctypes.data, Vc.ctypes.data if jobz else None, info.ctypes.data,
+            cnt.ctypes.data, int(nthreads), 0 if scheme == "exp" else 1)
+    if rc != 0:
+        raise ValueError(f"oracle: invalid arguments (n={n}, batch={batch})")
+    V = np.ascontiguousarray(np.swapaxes(Vc, 1, 2)) if jobz else None
+    return Result(W, V, info, int(cnt[0]), int(cnt[1]), int(cnt[2]))

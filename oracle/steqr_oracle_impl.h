@@ -370,6 +370,129 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort, int scheme,
     return 0;
 }
 
+/* 2-norm of x[0..m-1], scaled by the largest magnitude so that squares
+ * neither overflow nor underflow. */
+static real_t FN(nrm2)(int m, const real_t *x)
+{
+    real_t sc = 0;
+    for (int k = 0; k < m; ++k)
+        if (R_ABS(x[k]) > sc)
+            sc = R_ABS(x[k]);
+    if (sc == (real_t)0)
+        return (real_t)0;
+    real_t ss = 0;
+    for (int k = 0; k < m; ++k) {
+        real_t y = x[k] / sc;
+        ss += y * y;
+    }
+    return sc * R_SQRT(ss);
+}
+
+/*
+ * Dense symmetric A (n x n, column-major, lower triangle read) to tridiagonal
+ * form by Householder reflectors, the plain unblocked lower reduction: for
+ * i = 0 .. n-2 the reflector H_i = I - tau v v^T (v_{i+1} = 1, v_k = 0 for
+ * k <= i) annihilates A[i+2:n, i] and is applied from both sides to the
+ * trailing block, so T = Q^T A Q with Q = H_0 H_1 ... H_{n-2}.  The fused
+ * small-n syev (BatchLAS page "perf_steqr": sytrd, then the steqr solve, then
+ * the back-transform in one kernel) names this step; the pages give no
+ * formulas for it, so this is the standard form.  d[n], e[n-1] receive T;
+ * A is overwritten with the reflectors; Z (if not null) receives Q.
+ */
+static void FN(sytd2_lower)(int n, real_t *A, real_t *d, real_t *e, real_t *Z)
+{
+    real_t tau[64], v[64], p[64];
+    for (int i = 0; i + 1 < n; ++i) {
+        real_t *col = A + (size_t)i * n;
+        real_t alpha = col[i + 1];
+        real_t xnorm = FN(nrm2)(n - i - 2, col + i + 2);
+        real_t t = 0;
+        if (xnorm != (real_t)0) {
+            real_t beta = -R_COPYSIGN(FN(hypot2)(alpha, xnorm), alpha);
+            t = (beta - alpha) / beta;
+            real_t scal = (real_t)1 / (alpha - beta);
+            for (int k = i + 2; k < n; ++k)
+                col[k] = col[k] * scal;
+            alpha = beta;
+        }
+        e[i] = alpha;
+        tau[i] = t;
+        if (t != (real_t)0) {
+            v[i + 1] = 1;
+            for (int k = i + 2; k < n; ++k)
+                v[k] = col[k];
+            /* p = tau A22 v with A22 = A[i+1:n, i+1:n] (symmetric, lower) */
+            for (int r = i + 1; r < n; ++r) {
+                real_t acc = 0;
+                for (int c = i + 1; c < n; ++c) {
+                    real_t arc = r >= c ? A[r + (size_t)c * n] : A[c + (size_t)r * n];
+                    acc += arc * v[c];
+                }
+                p[r] = t * acc;
+            }
+            /* w = p - (tau/2) (p^T v) v;  A22 <- A22 - v w^T - w v^T */
+            real_t pv = 0;
+            for (int r = i + 1; r < n; ++r)
+                pv += p[r] * v[r];
+            real_t a2 = -(real_t)0.5 * t * pv;
+            for (int r = i + 1; r < n; ++r)
+                p[r] = p[r] + a2 * v[r];
+            for (int c = i + 1; c < n; ++c)
+                for (int r = c; r < n; ++r)
+                    A[r + (size_t)c * n] -= v[r] * p[c] + p[r] * v[c];
+        }
+        d[i] = A[i + (size_t)i * n];
+    }
+    d[n - 1] = A[(n - 1) + (size_t)(n - 1) * n];
+    if (Z) {
+        /* Q = H_0 (H_1 (... H_{n-2})): start from I and left-apply the
+         * reflectors last to first; H_i changes rows i+1.. of columns i+1.. */
+        for (int k = 0; k < n * n; ++k)
+            Z[k] = (k % (n + 1) == 0) ? (real_t)1 : (real_t)0;
+        for (int i = n - 2; i >= 0; --i) {
+            if (tau[i] == (real_t)0)
+                continue;
+            const real_t *col = A + (size_t)i * n;
+            v[i + 1] = 1;
+            for (int k = i + 2; k < n; ++k)
+                v[k] = col[k];
+            for (int c = i + 1; c < n; ++c) {
+                real_t s = 0;
+                for (int r = i + 1; r < n; ++r)
+                    s += v[r] * Z[r + (size_t)c * n];
+                s = s * tau[i];
+                for (int r = i + 1; r < n; ++r)
+                    Z[r + (size_t)c * n] -= s * v[r];
+            }
+        }
+    }
+}
+
+/* Fused small-n syev of one problem: reduction, then the steqr solve with the
+ * reduction's Q as the basis (back_transform).  A (n x n, column-major, lower
+ * read) is overwritten; W[n] receives the eigenvalues, V[n*n] (if jobz) the
+ * eigenvectors of A. */
+static int FN(syev_one)(int n, int jobz, int maxit_per_n, int sort, int scheme,
+                        real_t *A, real_t *W, real_t *V, real_t *ework, long *cnt)
+{
+    real_t e[64];
+    int bad = 0;
+    for (int c = 0; c < n; ++c)
+        for (int r = c; r < n; ++r)
+            if (!isfinite(A[r + (size_t)c * n]))
+                bad = 1;
+    if (bad) {
+        for (int k = 0; k < n; ++k)
+            W[k] = (real_t)NAN;
+        if (jobz)
+            for (int k = 0; k < n * n; ++k)
+                V[k] = (real_t)NAN;
+        return -1;
+    }
+    FN(sytd2_lower)(n, A, W, e, jobz ? V : (real_t *)0);
+    return FN(steqr_one)(n, jobz ? 2 : 0, maxit_per_n, sort, scheme, W, e, V, ework, cnt);
+}
+
 /* Batch driver arguments, one worker per contiguous slice of the batch. */
 typedef struct {
     int n, jobz, maxit_per_n, sort, scheme;
@@ -394,6 +517,74 @@ static void *FN(worker)(void *arg)
                                     db, eb, Qb, ework, jb->cnt);
     }
     return (void *)0;
+}
+
+typedef struct {
+    int n, jobz, maxit_per_n, sort, scheme;
+    long b0, b1;
+    real_t *A, *W, *V;
+    int *info;
+    long cnt[3];
+} FN(sjob_t);
+
+static void *FN(sworker)(void *arg)
+{
+    FN(sjob_t) *jb = (FN(sjob_t) *)arg;
+    const int n = jb->n;
+    real_t ework[64];
+    for (long b = jb->b0; b < jb->b1; ++b)
+        jb->info[b] = FN(syev_one)(n, jb->jobz, jb->maxit_per_n, jb->sort, jb->scheme,
+                                   jb->A + b * (long)n * n, jb->W + b * n,
+                                   jb->jobz ? jb->V + b * (long)n * n : (real_t *)0, ework, jb->cnt);
+    return (void *)0;
+}
+
+/* Fused syev of a batch (A: batch x n x n column-major, lower read and
+ * overwritten; W: batch x n; V: batch x n x n when jobz).  Same threading and
+ * counters as oracle_steqr_batch.  Returns 0, or -1 for invalid arguments. */
+int FN(oracle_syev_batch)(int n, long batch, int jobz, int maxit_per_n, int sort,
+                          real_t *A, real_t *W, real_t *V, int *info, long *counters,
+                          int nthreads, int scheme)
+{
+    if (n < 1 || n > 64 || batch < 0 || maxit_per_n < 0 || scheme < 0 || scheme > 1)
+        return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((long)nthreads > batch)
+        nthreads = batch > 0 ? (int)batch : 1;
+    FN(sjob_t) jobs[256];
+    pthread_t th[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].n = n;
+        jobs[t].jobz = jobz;
+        jobs[t].maxit_per_n = maxit_per_n;
+        jobs[t].sort = sort;
+        jobs[t].scheme = scheme;
+        jobs[t].b0 = batch * t / nthreads;
+        jobs[t].b1 = batch * (t + 1) / nthreads;
+        jobs[t].A = A;
+        jobs[t].W = W;
+        jobs[t].V = V;
+        jobs[t].info = info;
+        jobs[t].cnt[0] = jobs[t].cnt[1] = jobs[t].cnt[2] = 0;
+    }
+    if (nthreads == 1) {
+        FN(sworker)(&jobs[0]);
+    } else {
+        for (int t = 0; t < nthreads; ++t)
+            pthread_create(&th[t], (void *)0, FN(sworker), &jobs[t]);
+        for (int t = 0; t < nthreads; ++t)
+            pthread_join(th[t], (void *)0);
+    }
+    if (counters) {
+        counters[0] = counters[1] = counters[2] = 0;
+        for (int t = 0; t < nthreads; ++t)
+            for (int k = 0; k < 3; ++k)
+                counters[k] += jobs[t].cnt[k];
+    }
+    return 0;
 }
 
 /* Solve a batch of problems (d: batch x n, e: batch x (n-1), Q: batch x n x n

@@ -116,3 +116,15 @@ def orthogonal_bases(n: int, batch: int, dtype, seed: int = 0):
     sgn = np.sign(np.diagonal(R, axis1=1, axis2=2))
     sgn[sgn == 0] = 1.0
     return (Qf * sgn[:, None, :]).astype(dt)
+
+
+def dense_symmetric(n: int, batch: int, dtype, seed: int = 0):
+    """A (batch, n, n) symmetric with i.i.d. N(0,1) entries on and below the
+    diagonal (mirrored above), rounded to dtype: the dense input of the fused
+    small-n syev."""
+    dt = _as_dtype(dtype)
+    rng = np.random.default_rng(seed)
+    G = rng.standard_normal((batch, n, n))
+    L = np.tril(G)
+    A = L + np.swapaxes(np.tril(G, -1), 1, 2)
+    return A.astype(dt)

@@ -46,6 +46,12 @@ MUTATIONS = [
     ("pg_missing_fixup", "DD(lo) = DD(lo) - p;", "DD(lo) = DD(lo);"),
     ("pg_bulge_unscaled", "real_t f = sp * EE(i1), b = cp * EE(i1), rr;",
      "real_t f = EE(i1), b = cp * EE(i1), rr;"),
+    ("sytd2_rank1_only", "A[r + (size_t)c * n] -= v[r] * p[c] + p[r] * v[c];",
+     "A[r + (size_t)c * n] -= v[r] * p[c];"),
+    ("sytd2_beta_sign", "real_t beta = -R_COPYSIGN(FN(hypot2)(alpha, xnorm), alpha);",
+     "real_t beta = R_COPYSIGN(FN(hypot2)(alpha, xnorm), alpha);"),
+    ("sytd2_q_forward_order", "for (int i = n - 2; i >= 0; --i) {\n            if (tau[i] == (real_t)0)",
+     "for (int i = 0; i <= n - 2; ++i) {\n            if (tau[i] == (real_t)0)"),
 ]
 
 
@@ -129,6 +135,20 @@ def pin_failures(lib):
                 check(f"pg_res{n}", np.all(res <= 64 * n * eps * tn))
             else:
                 bad.append(f"pg_finite{n}")
+        # fused syev: eigenpairs of a dense symmetric matrix
+        for n in (6, 11):
+            A = inputs.dense_symmetric(n, 30, dt, seed=70 + n)
+            r = oracle.syev(A, jobz=True, lib=lib)
+            an = np.abs(A.astype(np.float64)).sum(1).max(1)
+            ref = np.linalg.eigvalsh(A.astype(np.float64))
+            lam = np.nan_to_num(r.lam.astype(np.float64), nan=1e300)
+            check(f"syev_lam{n}", np.all(np.abs(lam - ref).max(1) <= 16 * n * eps * an))
+            if np.all(np.isfinite(r.Q)):
+                V = r.Q.astype(np.float64)
+                res = np.abs(A.astype(np.float64) @ V - V * r.lam[:, None, :]).reshape(30, -1).max(1)
+                check(f"syev_res{n}", np.all(res <= 64 * n * eps * an))
+            else:
+                bad.append(f"syev_finite{n}")
         # back_transform: the rotations are right-applied to an orthogonal Z,
         # so Z Q holds the eigenvectors of Z T Z^T
         d, e = inputs.normal_problems(7, 20, dt, seed=6)

@@ -464,3 +464,74 @@ def test_pg_scheme_toeplitz_and_hard_cases(dt):
     tn = H.norm1(dm, em).astype(np.float64)
     ok = np.isfinite(ex.lam).all(1)
     assert np.all(np.abs(pg.lam[ok].astype(np.float64) - ex.lam[ok]).max(1) <= 2 * H.lam_tol(32, dt, tn[ok]))
+
+
+# --- fused small-n syev (BatchLAS page "perf_steqr": the fused kernel runs
+# the reduction to tridiagonal form, the steqr solve and the back-transform;
+# the reduction is the plain Householder one) ---
+
+def _dense_checks(A, r, dt):
+    n = A.shape[1]
+    eps = H.eps_of(dt)
+    Ad = np.asarray(A, dtype=np.longdouble)
+    an = np.abs(Ad).sum(1).max(1).astype(np.float64)
+    ref = np.linalg.eigvalsh(A.astype(np.float64))
+    assert np.all(np.abs(r.lam.astype(np.float64) - ref).max(1) <= 16 * n * eps * an)
+    if r.Q is not None:
+        V = np.asarray(r.Q, dtype=np.longdouble)
+        R = Ad @ V - V * np.asarray(r.lam, dtype=np.longdouble)[:, None, :]
+        O = np.swapaxes(V, 1, 2) @ V - np.eye(n, dtype=np.longdouble)
+        assert np.all(np.abs(R).reshape(len(A), -1).max(1).astype(np.float64) <= 64 * n * eps * an)
+        assert np.abs(O).max() <= 64 * n * eps
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+@pytest.mark.parametrize("n", [1, 2, 5, 12, 16, 31, 64])
+def test_syev_against_library_and_residual(dt, n):
+    A = inputs.dense_symmetric(n, 120, dt, seed=90 + n)
+    r = oracle.syev(A, jobz=True)
+    assert np.all(r.info == 0)
+    _dense_checks(A, r, dt)
+    rn = oracle.syev(A, jobz=False)
+    np.testing.assert_array_equal(rn.lam, r.lam)
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_syev_of_a_tridiagonal_matrix_is_steqr_bitwise(dt):
+    """A reflector has nothing to annihilate below the subdiagonal, so the
+    reduction returns d and e untouched and Q = I."""
+    n = 13
+    d, e = inputs.normal_problems(n, 80, dt, seed=91)
+    A = H.dense(d, e, dtype=dt)
+    a = oracle.syev(A, jobz=True)
+    b = oracle.steqr(d, e, jobz=True)
+    np.testing.assert_array_equal(a.lam, b.lam)
+    np.testing.assert_array_equal(a.Q, b.Q)
+    np.testing.assert_array_equal(a.info, b.info)
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_syev_degenerate_inputs(dt):
+    n = 9
+    rng = np.random.default_rng(4)
+    diag = rng.standard_normal((10, n)).astype(dt)
+    A = np.zeros((10, n, n), dtype=dt)
+    A[:, np.arange(n), np.arange(n)] = diag
+    r = oracle.syev(A, jobz=True)
+    np.testing.assert_array_equal(r.lam, np.sort(diag, axis=1))
+    assert np.all(np.isin(r.Q, (-1, 0, 1)))
+    z = oracle.syev(np.zeros((3, n, n), dtype=dt), jobz=True)
+    assert np.all(z.lam == 0) and np.all(z.Q == np.eye(n, dtype=dt))
+    # only the lower triangle is read: NaN above it changes nothing, below it
+    # poisons the problem
+    A = inputs.dense_symmetric(n, 4, dt, seed=5)
+    ref = oracle.syev(A, jobz=True)
+    Au = A.copy()
+    Au[0, 1, 5] = np.nan
+    up = oracle.syev(Au, jobz=True)
+    np.testing.assert_array_equal(up.lam, ref.lam)
+    Al = A.copy()
+    Al[1, 5, 1] = np.nan
+    lo = oracle.syev(Al, jobz=True)
+    assert lo.info[1] == -1 and np.all(np.isnan(lo.lam[1])) and np.all(np.isnan(lo.Q[1]))
+    np.testing.assert_array_equal(lo.lam[0], ref.lam[0])
