@@ -202,6 +202,32 @@ int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
                        void *d, const void *e, void *Q, int32_t *info,
                        void *stream, const bstq_params *p);
 
+/*
+ * Fused small-n dense symmetric eigensolver (BatchLAS page "perf_steqr": the
+ * fused syev kernel runs the reduction to tridiagonal form, the steqr solve
+ * and the back-transform in one launch).  One lane per problem: the lower
+ * triangle of A is reduced by Householder reflectors (T = Q^T A Q), T is
+ * solved with Q as the basis (as back_transform), so the eigenvectors come
+ * out as those of A.  1 <= n <= 32.
+ *   A     in      batch*n*n values, column-major per problem
+ *                 (A[b*n*n + j*n + i] = A_ij); only i >= j is read.
+ *   W     out     batch*n eigenvalues, ascending per problem.
+ *   V     out     batch*n*n values when jobz == V (column j the eigenvector
+ *                 of W[j]); ignored (may be NULL) for jobz == N.
+ *   work  in/out  bstq_syev_work_size(...) bytes, 256-byte aligned; int32
+ *                 info[batch] at offset 0 (0, k > 0 budget exhausted, -1 a
+ *                 non-finite entry in the lower triangle).
+ *   p     optional: no_sort, max_sweeps_per_n, scheduler, update_scheme and
+ *                 threads_per_block apply; back_transform, qstore or a kernel
+ *                 other than DYNAMIC return -10.
+ * Returns 0 or -k as bstq_solve_ex (-5 A, -6 W, -7 V, -8 work, -3 n > 32).
+ */
+size_t bstq_syev_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                           const bstq_params *p);
+
+int bstq_syev(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const void *A,
+              void *W, void *V, void *work, void *stream, const bstq_params *p);
+
 /* Description of the kernel the library would launch (for tests and
  * benchmarks): fills up to `len` bytes of `buf` with a NUL-terminated string
  * such as "lane<f32,16,V,shared,flat> tpb=224 grid=147" and returns 0, or

@@ -27,7 +27,8 @@ MAX_N = 64
 # Every symbol include/bstq.h declares.
 EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",
            "bstq_host_work_size", "bstq_solve_host", "bstq_describe",
-           "bstq_status_string", "bstq_version", "bstq_last_error", "bstq_solve_noalloc")
+           "bstq_status_string", "bstq_version", "bstq_last_error", "bstq_solve_noalloc",
+           "bstq_syev_work_size", "bstq_syev")
 
 
 class Params(ctypes.Structure):
@@ -85,6 +86,10 @@ def load(path: str = LIB_PATH):
         lib.bstq_version.argtypes = []
         lib.bstq_last_error.restype = ctypes.c_char_p
         lib.bstq_last_error.argtypes = []
+        lib.bstq_syev_work_size.restype = sz
+        lib.bstq_syev_work_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P]
+        lib.bstq_syev.restype = ctypes.c_int
+        lib.bstq_syev.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp, vp, P]
         lib.bstq_solve_noalloc.restype = ctypes.c_int
         lib.bstq_solve_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp,
                                            vp, P]
@@ -222,3 +227,40 @@ def solve_noalloc(d, e, Q, info, stream=None, **params):
     if rc != 0:
         raise BstqError(rc, "bstq_solve_noalloc")
     return d, Q.transpose(1, 2), info
+
+
+def syev_work_size(dtype, jobz: bool, n: int, batch: int, **params) -> int:
+    p = _params(**params)
+    return int(load().bstq_syev_work_size(_dtype_code(dtype), int(bool(jobz)), int(n), int(batch),
+                                          ctypes.byref(p)))
+
+
+def syev(A, jobz: bool = True, work=None, stream=None, **params):
+    """Fused small-n dense symmetric eigensolver on a CUDA tensor ``A``
+    (batch, n, n), n <= 32, of which the lower triangle (A[b, i, j], i >= j)
+    is read.  Returns (W, V, info): eigenvalues (batch, n) ascending,
+    eigenvectors (batch, n, n) with V[b, :, j] that of W[b, j] (None for
+    jobz N), info (batch,) int32.  Nothing is synchronised."""
+    import torch
+    if not A.is_cuda or A.dim() != 3 or A.shape[1] != A.shape[2]:
+        raise ValueError("bstq.syev: A must be a (batch, n, n) CUDA tensor")
+    batch, n, _ = A.shape
+    code = _dtype_code(A.dtype)
+    Ac = A.transpose(1, 2).contiguous()  # library layout: memory [b][j][i] = A_ij
+    W = torch.empty((batch, n), dtype=A.dtype, device=A.device)
+    Vs = torch.empty((batch, n, n), dtype=A.dtype, device=A.device) if jobz else None
+    p = _params(**params)
+    lib = load()
+    wbytes = int(lib.bstq_syev_work_size(code, int(bool(jobz)), int(n), int(batch), ctypes.byref(p)))
+    if wbytes == 0:
+        raise BstqError(-10, "bstq_syev_work_size")
+    if work is None:
+        work = torch.empty(wbytes, dtype=torch.uint8, device=A.device)
+    elif work.numel() * work.element_size() < wbytes:
+        raise ValueError(f"bstq.syev: work needs {wbytes} bytes")
+    rc = lib.bstq_syev(code, int(bool(jobz)), int(n), int(batch), Ac.data_ptr(), W.data_ptr(),
+                       Vs.data_ptr() if jobz else None, work.data_ptr(), _stream_handle(stream), ctypes.byref(p))
+    if rc != 0:
+        raise BstqError(rc, "bstq_syev")
+    info = work[: 4 * batch].view(torch.int32)
+    return W, (Vs.transpose(1, 2) if jobz else None), info

@@ -26,6 +26,7 @@ struct Plan {
 };
 
 constexpr int kNmList[] = {4, 8, 12, 16, 24, 32, 48, 64};
+constexpr int kSyevMaxN = 32;  // the fused syev kernels are built up to n = 32
 
 thread_local char g_last_error[256] = "";
 
@@ -179,7 +180,7 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
 
 // Build the launch plan.  Returns 0, -10 for parameters no kernel supports,
 // or BSTQ_ERR_NODEVICE.
-int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p, Plan &pl)
+int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p, Plan &pl, int force_family = 0)
 {
     DevInfo di;
     if (!dev_info(di))
@@ -191,12 +192,13 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
             break;
         }
     const bool pg = p && p->update_scheme == 1;
-    const int family = (p && p->kernel) ? p->kernel : (pg ? FAMILY_DYNAMIC : default_family(dtype, jobz, nm));
-    if (pg && family != FAMILY_DYNAMIC)
+    const int family = force_family ? force_family
+                                    : (p && p->kernel) ? p->kernel : (pg ? FAMILY_DYNAMIC : default_family(dtype, jobz, nm));
+    if (pg && family == FAMILY_STATIC)
         return -10;  // the PG step runs in the dynamic-position kernels only
     const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
     int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm, sched)) : 0;
-    if (family == FAMILY_DYNAMIC && jobz)
+    if (family != FAMILY_STATIC && jobz)
         qs = QS_GLOBAL;  // the dynamic kernels keep Q in global scratch
     pl.k = find_entry(dtype, jobz, nm, qs, sched, family);
     if (!pl.k)
@@ -309,7 +311,7 @@ const char *qs_name(int qs)
 int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const void *e, void *Q,
            void *work, cudaStream_t st, const bstq_params *p)
 {
-    KParams kp;
+    KParams kp{};
     kp.d = d;
     kp.e = e;
     kp.Q = Q;
@@ -453,6 +455,103 @@ extern "C" int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t 
     return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Fused small-n syev.  Workspace: info[batch] | Q scratch of the solve |
+// off-diagonal scratch batch x (n-1) | the reduction's scratch (grid x tpb x
+// n x n), each 256-byte aligned.
+// ---------------------------------------------------------------------------
+namespace bstq {
+namespace {
+
+struct SyevPlan {
+    Plan pl;
+    size_t off_q = 0, off_e = 0, off_s = 0, total = 0;
+};
+
+int make_syev_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p, SyevPlan &sp)
+{
+    if (n > kSyevMaxN)
+        return -3;
+    if (p && (p->back_transform || p->qstore || (p->kernel && p->kernel != BSTQ_KERNEL_DYNAMIC)))
+        return -10;  // the fused kernel is one form; these do not apply
+    int rc = make_plan(dtype, jobz, n, batch, p, sp.pl, FAMILY_SYEV);
+    if (rc)
+        return rc;
+    const size_t elem = dtype ? 8 : 4;
+    sp.off_q = align256(size_t(batch) * 4);
+    sp.off_e = sp.off_q + align256(sp.pl.qwork_bytes);
+    sp.off_s = sp.off_e + align256(elem * size_t(n > 1 ? n - 1 : 1) * size_t(batch));
+    sp.total = sp.off_s + align256(elem * size_t(n) * n * size_t(sp.pl.tpb) * size_t(sp.pl.grid));
+    return 0;
+}
+
+}  // namespace
+}  // namespace bstq
+
+extern "C" size_t bstq_syev_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
+                                      const bstq_params *p)
+{
+    if (check_args(dtype, jobz, n, batch, p) != 0)
+        return 0;
+    SyevPlan sp;
+    if (make_syev_plan(dtype, jobz, n, batch, p, sp) != 0)
+        return 0;
+    return sp.total > 256 ? sp.total : 256;
+}
+
+extern "C" int bstq_syev(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const void *A, void *W,
+                         void *V, void *work, void *stream, const bstq_params *p)
+{
+    int rc = check_args(dtype, jobz, n, batch, p);
+    if (rc)
+        return rc;
+    if (n > kSyevMaxN)
+        return -3;
+    if (batch == 0)
+        return 0;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    if (!A || misaligned(A, elem))
+        return -5;
+    if (!W || misaligned(W, elem))
+        return -6;
+    if (jobz == BSTQ_JOBZ_V && (!V || misaligned(V, elem)))
+        return -7;
+    if (!work || misaligned(work, 256))
+        return -8;
+    SyevPlan sp;
+    rc = make_syev_plan(dtype, jobz, n, batch, p, sp);
+    if (rc)
+        return rc;
+    const Plan &pl = sp.pl;
+    char *w = reinterpret_cast<char *>(work);
+    KParams kp{};
+    kp.d = W;
+    kp.e = w + sp.off_e;
+    kp.Q = jobz == BSTQ_JOBZ_V ? V : nullptr;
+    kp.info = reinterpret_cast<int *>(w);
+    kp.qwork = pl.qwork_bytes ? w + sp.off_q : nullptr;
+    kp.batch = batch;
+    kp.n = n;
+    kp.budget = ((p && p->max_sweeps_per_n) ? p->max_sweeps_per_n : 30) * n;
+    kp.sort = (p && p->no_sort) ? 0 : 1;
+    kp.ppb = pl.ppb;
+    kp.back = 0;  // the kernel sets it for its solve
+    kp.scheme = (p && p->update_scheme) ? 1 : 0;
+    kp.A = A;
+    kp.sscr = w + sp.off_s;
+    if (pl.smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "cudaFuncSetAttribute");
+    }
+    void *args[] = {&kp};
+    if (pl.grid > 0x7fffffffLL)
+        return -4;
+    cudaError_t err = cudaLaunchKernel(pl.k->fn, dim3((unsigned)pl.grid), dim3(pl.tpb), args, pl.smem,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? 0 : cuda_fail(err, "cudaLaunchKernel");
+}
+
 extern "C" int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const bstq_params *p,
                              char *buf, size_t len)
 {
@@ -589,7 +688,7 @@ extern "C" int bstq_solve_noalloc(bstq_dtype dtype, bstq_jobz jobz, int n, int64
     rc = noalloc_scratch(&scratch);
     if (rc)
         return rc;
-    KParams kp;
+    KParams kp{};
     kp.d = d;
     kp.e = e;
     kp.Q = Q;

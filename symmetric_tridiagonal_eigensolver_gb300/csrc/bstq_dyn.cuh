@@ -624,8 +624,11 @@ struct DynLane {
     }
 };
 
+// The whole solve of one lane's problem (load, the settle/chase loop under
+// the chosen scheduler, the sorted store); dyn_kernel and the fused syev
+// kernel both run it.
 template <typename T, int NM, bool WANTZ, int SCHED>
-__global__ void dyn_kernel(KParams p)
+__device__ __forceinline__ void dyn_body(const KParams &p)
 {
     extern __shared__ uint4 smem_raw[];
     using LaneT = DynLane<T, NM, WANTZ>;
@@ -815,6 +818,12 @@ __global__ void dyn_kernel(KParams p)
         }
     }
     p.info[b] = (L.status == ST_FAIL) ? L.info : 0;
+}
+
+template <typename T, int NM, bool WANTZ, int SCHED>
+__global__ void dyn_kernel(KParams p)
+{
+    dyn_body<T, NM, WANTZ, SCHED>(p);
 }
 
 }  // namespace bstq

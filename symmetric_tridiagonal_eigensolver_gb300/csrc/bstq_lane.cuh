@@ -54,6 +54,8 @@ struct KParams {
     int ppb;           // problems per block (split-role kernel)
     int back;          // 1: Q holds the basis Z on entry (back_transform)
     int scheme;        // 0 EXP, 1 PG update (dynamic-position kernels)
+    const void *A;     // fused syev: dense input, batch x n x n
+    void *sscr;        // fused syev: the reduction's scratch
 };
 
 // ---------------------------------------------------------------------------

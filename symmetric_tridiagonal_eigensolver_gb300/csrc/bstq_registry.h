@@ -13,10 +13,11 @@ struct KernelEntry {
     int qs;      // Q storage (QS_*; 0 for jobz N)
     int sched;   // SCHED_FLAT / SCHED_NESTED
     const void *fn;
-    int family;  // FAMILY_STATIC (bstq_lane.cuh) / FAMILY_DYNAMIC (bstq_dyn.cuh)
+    int family;  // FAMILY_STATIC (bstq_lane.cuh) / FAMILY_DYNAMIC (bstq_dyn.cuh) /
+                 // FAMILY_SYEV (bstq_syev.cuh, fused dense solve)
 };
 
-enum { FAMILY_STATIC = 1, FAMILY_DYNAMIC = 2 };
+enum { FAMILY_STATIC = 1, FAMILY_DYNAMIC = 2, FAMILY_SYEV = 3 };
 
 #define BSTQ_DECLARE_UNIT(name) const KernelEntry *entries_##name(int *count);
 BSTQ_FOR_EACH_UNIT(BSTQ_DECLARE_UNIT)
