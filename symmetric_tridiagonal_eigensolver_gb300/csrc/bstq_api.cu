@@ -458,7 +458,7 @@ extern "C" int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t 
 // ---------------------------------------------------------------------------
 // Fused small-n syev.  Workspace: info[batch] | Q scratch of the solve |
 // off-diagonal scratch batch x (n-1) | the reduction's scratch (grid x tpb x
-// n x n), each 256-byte aligned.
+// 2 n^2: the copy of A and the reduction's Q), each 256-byte aligned.
 // ---------------------------------------------------------------------------
 namespace bstq {
 namespace {
@@ -481,7 +481,7 @@ int make_syev_plan(int dtype, int jobz, int n, long long batch, const bstq_param
     sp.off_q = align256(size_t(batch) * 4);
     sp.off_e = sp.off_q + align256(sp.pl.qwork_bytes);
     sp.off_s = sp.off_e + align256(elem * size_t(n > 1 ? n - 1 : 1) * size_t(batch));
-    sp.total = sp.off_s + align256(elem * size_t(n) * n * size_t(sp.pl.tpb) * size_t(sp.pl.grid));
+    sp.total = sp.off_s + align256(elem * 2 * size_t(n) * n * size_t(sp.pl.tpb) * size_t(sp.pl.grid));
     return 0;
 }
 

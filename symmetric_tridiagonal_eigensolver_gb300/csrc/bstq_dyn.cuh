@@ -55,6 +55,20 @@ struct DynQ {
             base[(k * G + g) * stride] = V16{x[2 * g], x[2 * g + 1]};
     }
     __device__ __forceinline__ V16 &vec(int k, int g) const { return base[(k * G + g) * stride]; }
+    // Column s from a basis stored interleaved: row r at zc[r * st] (the
+    // fused syev's reduction), zero below n.
+    __device__ __forceinline__ void init_col_strided(int s, const T *zc, int st, int n) const
+    {
+        T col[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            col[r] = r < n ? zc[(size_t)r * st] : T(0);
+        E x[NE];
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+            x[j] = Tr::pack(&col[j * RPE]);
+        store(s, x);
+    }
     // Column s from the caller's basis: rows 0 .. n-1 of zc, zero below
     // (back_transform).
     __device__ __forceinline__ void init_col_from(int s, const T *zc, int n, bool vec) const
@@ -659,7 +673,13 @@ __device__ __forceinline__ void dyn_body(const KParams &p)
             for (int s = 0; s < NM; ++s) {
                 // column phys(s) of the identity, or of the caller's basis
                 // with back_transform
-                if (p.back && s < L.n)
+                if (p.back == 2 && s < L.n)  // fused syev: Q of the reduction
+                    L.q.init_col_strided(s,
+                                         reinterpret_cast<const T *>(p.sscr) +
+                                             ((size_t)blockIdx.x * 2 + 1) * L.n * L.n * tpb + threadIdx.x +
+                                             (size_t)L.phys(s) * L.n * tpb,
+                                         tpb, L.n);
+                else if (p.back && s < L.n)
                     L.q.init_col_from(s, zb + (long long)L.phys(s) * L.n, L.n, zvec);
                 else
                     L.q.init_col(s, s < L.n ? L.phys(s) : s);

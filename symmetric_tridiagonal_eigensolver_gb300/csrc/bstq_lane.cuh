@@ -52,7 +52,8 @@ struct KParams {
     int budget;        // sweep budget per problem (max_sweeps_per_n * n)
     int sort;          // 1: ascending output
     int ppb;           // problems per block (split-role kernel)
-    int back;          // 1: Q holds the basis Z on entry (back_transform)
+    int back;          // 1: Q holds the basis Z on entry (back_transform);
+                       // 2: the basis is the fused syev's, in sscr
     int scheme;        // 0 EXP, 1 PG update (dynamic-position kernels)
     const void *A;     // fused syev: dense input, batch x n x n
     void *sscr;        // fused syev: the reduction's scratch

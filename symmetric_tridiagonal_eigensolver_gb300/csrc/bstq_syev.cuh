@@ -24,10 +24,13 @@
 
 namespace bstq {
 
+// Z (if WANTZ) is written interleaved like S: element (r, c) at
+// Z[(r + c n) * st].
 template <typename T, int NM, bool WANTZ>
 __device__ void sytd2_lane(int n, const T *A, T *S, int st, T *d, T *e, T *Z)
 {
     auto s_at = [&](int r, int c) -> T & { return S[(size_t)(r + c * n) * st]; };
+    auto z_at = [&](int r, int c) -> T & { return Z[(size_t)(r + c * n) * st]; };
     bool bad = false;
     for (int c = 0; c < n; ++c)
         for (int r = c; r < n; ++r) {
@@ -100,7 +103,7 @@ __device__ void sytd2_lane(int n, const T *A, T *S, int st, T *d, T *e, T *Z)
         // left-applied last to first; H_i changes rows and columns i+1..
         for (int c = 0; c < n; ++c)
             for (int r = 0; r < n; ++r)
-                Z[r + (size_t)c * n] = r == c ? T(1) : T(0);
+                z_at(r, c) = r == c ? T(1) : T(0);
         for (int i = n - 2; i >= 0; --i) {
             if (tau[i] == T(0))
                 continue;
@@ -110,10 +113,10 @@ __device__ void sytd2_lane(int n, const T *A, T *S, int st, T *d, T *e, T *Z)
             for (int c = i + 1; c < n; ++c) {
                 T sum = T(0);
                 for (int r = i + 1; r < n; ++r)
-                    sum = fma(v[r], Z[r + (size_t)c * n], sum);
+                    sum = fma(v[r], z_at(r, c), sum);
                 sum = sum * tau[i];
                 for (int r = i + 1; r < n; ++r)
-                    Z[r + (size_t)c * n] = fma(-sum, v[r], Z[r + (size_t)c * n]);
+                    z_at(r, c) = fma(-sum, v[r], z_at(r, c));
             }
         }
     }
@@ -121,8 +124,9 @@ __device__ void sytd2_lane(int n, const T *A, T *S, int st, T *d, T *e, T *Z)
 
 // p.A: batch x n x n dense input (column-major per problem, lower triangle
 // read); p.d: the eigenvalues out; p.e: batch x (n-1) scratch for the
-// off-diagonal; p.Q: the eigenvectors out (jobz V; it carries Q of the
-// reduction into the solve); p.sscr: the reduction's scratch.
+// off-diagonal; p.Q: the eigenvectors out (jobz V); p.sscr: per block
+// 2 n^2 x blockDim elements, the reduction's copy of A, then Q of the
+// reduction (both interleaved), which the solve takes as its basis.
 template <typename T, int NM, bool WANTZ, int SCHED>
 __global__ void syev_kernel(KParams p)
 {
@@ -130,14 +134,14 @@ __global__ void syev_kernel(KParams p)
     const long long b = (long long)blockIdx.x * tpb + threadIdx.x;
     const int n = p.n;
     if (b < p.batch) {
-        T *S = reinterpret_cast<T *>(p.sscr) + (size_t)blockIdx.x * n * n * tpb + threadIdx.x;
+        T *S = reinterpret_cast<T *>(p.sscr) + (size_t)blockIdx.x * 2 * n * n * tpb + threadIdx.x;
         sytd2_lane<T, NM, WANTZ>(n, reinterpret_cast<const T *>(p.A) + b * (long long)n * n, S, tpb,
                                  reinterpret_cast<T *>(p.d) + b * n,
                                  reinterpret_cast<T *>(const_cast<void *>(p.e)) + b * (n - 1),
-                                 WANTZ ? reinterpret_cast<T *>(p.Q) + b * (long long)n * n : nullptr);
+                                 S + (size_t)n * n * tpb);
     }
     KParams q = p;
-    q.back = WANTZ ? 1 : 0;
+    q.back = WANTZ ? 2 : 0;  // basis from the interleaved scratch
     dyn_body<T, NM, WANTZ, SCHED>(q);
 }
 
