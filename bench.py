@@ -49,8 +49,8 @@ PAGES_BASELINE = 32768 / 450.9e-6
 # (kernel_digest()); a changed kernel no longer matches and reports null
 # (profiles/split_f32_n16_V_batch32768.md).
 NCU_TRAFFIC = {
-    ("lane<f32,16,V,split,flat> tpb=512 grid=152 smem=207984 regs=128 work=131072", "cb4cccc46dcf2b9d"):
-        4.2752e6 + 0.144384e6,
+    ("lane<f32,16,V,split,flat> tpb=512 grid=152 smem=207984 regs=128 work=131072", "52a19c0d673a751e"):
+        4.303616e6 + 0.212224e6,
 }
 
 
@@ -227,6 +227,29 @@ def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, min_war
     return ms, d, e, desc
 
 
+def time_syev(n, batch, dtype, jobz, steps, warmup, flush, stream):
+    """Device-side timing of the fused small-n syev (dense symmetric A, N(0,1)
+    entries on and below the diagonal, seed 0): ms per call."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    dt = np.float32 if dtype == "float32" else np.float64
+    A = torch.from_numpy(inputs.dense_symmetric(n, batch, dt, seed=0)).cuda()
+    work = torch.empty(bstq.syev_work_size(dt, jobz, n, batch), dtype=torch.uint8, device="cuda")
+    times = []
+    with torch.cuda.stream(stream):
+        for it in range(warmup + steps):
+            flush.zero_()
+            s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            W, V, info = bstq.syev(A, jobz=jobz, work=work, stream=stream)
+            t.record(stream)
+            if it >= warmup:
+                times.append((s, t))
+        torch.cuda.synchronize()
+    assert int((info != 0).sum()) == 0, "unconverged problems in the syev batch"
+    return statistics.mean(s.elapsed_time(t) for s, t in times)
+
+
 def time_e2e(w, steps, warmup, stream):
     """End to end through the C ABI on pinned host buffers: H2D of d and e,
     the solve, D2H of lambda, Q and info, per step."""
@@ -389,6 +412,11 @@ def main():
             workloads[wl_name(w)] = {"problems_per_s": w["batch"] / t, "ms": t * 1e3,
                                      "roofline_fraction": roof_t / t, "kernel": wdesc,
                                      "gflop": fl / 1e9, "mb": by / 1e6}
+        for dtype, n in (("float32", 16), ("float64", 12)):
+            ms_s = time_syev(n, 32768, dtype, True, max(5, args.steps // 2), 3, flush, stream)
+            workloads[f"fused syev {dtype} n={n} jobz=V batch=32768 dense N(0,1) seed 0"] = {
+                "problems_per_s": 32768 / (ms_s / 1e3), "ms": ms_s,
+                "kernel": "syev_kernel (Householder reduction + dynamic-position solve, one launch)"}
 
     if rank != 0:
         if world > 1:
