@@ -174,7 +174,9 @@ def test_unaligned_q_matches_aligned(dt, n, params):
                                          (np.float32, 32, {}), (np.float32, 16, {"kernel": 2}),
                                          (np.float32, 16, {"qstore": 3}), (np.float64, 12, {}),
                                          (np.float64, 7, {}), (np.float64, 8, {"kernel": 1}),
-                                         (np.float64, 32, {})])
+                                         (np.float64, 32, {}), (np.float32, 16, {"scheduler": 2}),
+                                         (np.float64, 12, {"scheduler": 2}), (np.float64, 12, {"update_scheme": 1}),
+                                         (np.float32, 40, {}), (np.float64, 64, {})])
 def test_back_transform_matches_oracle(dt, n, params):
     """back_transform (BatchLAS page "algo_steqr", eigenvector accumulation):
     the rotations are right-applied to the caller's basis Z.  With Z

@@ -17,7 +17,8 @@ from tests.gpu_helpers import orth_err, run_gpu, tri_residual
 pytestmark = pytest.mark.gpu
 
 CASES = [(np.float64, 12, 3000), (np.float32, 16, 2000), (np.float64, 32, 700), (np.float32, 29, 1100),
-         (np.float32, 8, 3000), (np.float64, 5, 2500), (np.float32, 1, 300)]
+         (np.float32, 8, 3000), (np.float64, 5, 2500), (np.float32, 1, 300), (np.float32, 48, 700),
+         (np.float64, 40, 300)]
 
 
 def _noalloc(d, e):
