@@ -180,3 +180,80 @@ def syev(A, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N, sort: boo
         raise ValueError(f"oracle: invalid arguments (n={n}, batch={batch})")
     V = np.ascontiguousarray(np.swapaxes(Vc, 1, 2)) if jobz else None
     return Result(W, V, info, int(cnt[0]), int(cnt[1]), int(cnt[2]))
+
+
+class Leaves:
+    """Oracle output of the stedc leaf solve for a batch of size-n problems
+    torn into leaves: ``starts``/``sizes`` the leaves' first rows and sizes
+    (consecutive leaves of ``leaf`` rows, the remainder last), ``d_torn``
+    (batch, n) the torn diagonal, ``lam`` (batch, n) each leaf's eigenvalues
+    at the leaf's rows (ascending within the leaf), ``Q`` a list with one
+    (batch, size, size) array per leaf (``Q[k][b, :, j]`` the j-th
+    eigenvector of leaf k, None when jobz = N) and ``info`` (batch, leaves)."""
+
+    def __init__(self, starts, sizes, d_torn, lam, Q, info):
+        self.starts = starts
+        self.sizes = sizes
+        self.d_torn = d_torn
+        self.lam = lam
+        self.Q = Q
+        self.info = info
+
+
+def leaf_partition(n: int, leaf: int):
+    """Leaves of a size-n problem: consecutive runs of ``leaf`` rows from the
+    top, the remainder (if any) as a last, shorter leaf.  A leaf size at or
+    above n gives one leaf.  Returns (starts, sizes)."""
+    if n < 1 or leaf < 1:
+        raise ValueError("oracle: n and leaf must be >= 1")
+    size = min(leaf, n)
+    starts = list(range(0, n, size))
+    return starts, [min(size, n - s) for s in starts]
+
+
+def tear(d, e, leaf: int):
+    """The divide step of divide and conquer (BatchLAS page "algo_steqr": the
+    leaf solve of stedc; the rank-one tear of Cuppen's method): at every
+    boundary between leaves, rows r-1 | r with off-diagonal beta = e[r-1],
+    T = diag(T_1, T_2) + |beta| v v^T with v = e_{r-1} + sign(beta) e_r, so
+    the leaves are T's diagonal blocks with |beta| taken off the two diagonal
+    entries next to the boundary.  Boundaries are applied top to bottom in
+    the problem's own precision, so a one-row leaf between two boundaries
+    holds (d - |e_left|) - |e_right|.  Returns (starts, sizes, d_torn)."""
+    d = np.asarray(d)
+    batch, n = d.shape
+    e = np.asarray(e, dtype=d.dtype).reshape(batch, max(n - 1, 0))
+    starts, sizes = leaf_partition(n, leaf)
+    dt = d.copy()
+    for r in starts[1:]:
+        beta = np.abs(e[:, r - 1])
+        dt[:, r - 1] = dt[:, r - 1] - beta
+        dt[:, r] = dt[:, r] - beta
+    return starts, sizes, dt
+
+
+def stedc_leaves(d, e, leaf: int, jobz: bool = True, maxit_per_n: int = DEFAULT_MAXIT_PER_N,
+                 sort: bool = True, nthreads: int = 1, lib=None) -> Leaves:
+    """Leaf solve of divide and conquer on host arrays ``d`` (batch, n) and
+    ``e`` (batch, n-1): tear every problem into leaves (``tear``), then solve
+    each leaf, a tridiagonal problem of at most ``leaf`` rows whose
+    off-diagonal is e inside the leaf, with the steqr oracle (identity start,
+    ascending eigenvalues).  Inputs are not modified."""
+    d = np.asarray(d)
+    if d.dtype not in (np.float32, np.float64):
+        raise TypeError("oracle: d must be float32 or float64")
+    if d.ndim == 1:
+        d = d[None, :]
+    batch, n = d.shape
+    e = np.asarray(e, dtype=d.dtype).reshape(batch, max(n - 1, 0))
+    starts, sizes, dt = tear(d, e, leaf)
+    lam = np.empty_like(dt)
+    info = np.zeros((batch, len(starts)), dtype=np.int32)
+    Qs = []
+    for k, (s, m) in enumerate(zip(starts, sizes)):
+        r = steqr(dt[:, s:s + m], e[:, s:s + m - 1], jobz=jobz, maxit_per_n=maxit_per_n, sort=sort,
+                  nthreads=nthreads, lib=lib)
+        lam[:, s:s + m] = r.lam
+        info[:, k] = r.info
+        Qs.append(r.Q)
+    return Leaves(starts, sizes, dt, lam, Qs if jobz else None, info)
