@@ -250,6 +250,35 @@ def time_syev(n, batch, dtype, jobz, steps, warmup, flush, stream):
     return statistics.mean(s.elapsed_time(t) for s, t in times)
 
 
+def time_leaves(n, leaf, batch, dtype, jobz, steps, warmup, flush, stream):
+    """Device-side timing of the stedc leaf solve (tear, the batched leaf
+    solves and the gather, all in the call) on N(0,1) d and e, seed 0:
+    ms per call."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    dt = np.float32 if dtype == "float32" else np.float64
+    d, e = inputs.normal_problems(n, batch, dt, seed=0)
+    d0 = torch.from_numpy(d).cuda()
+    dg = torch.empty_like(d0)
+    eg = torch.from_numpy(e).cuda()
+    work = torch.empty(int(bstq.load().bstq_stedc_leaves_work_size(bstq._dtype_code(dt), int(jobz), n, leaf, batch,
+                                                                   None)), dtype=torch.uint8, device="cuda")
+    times = []
+    with torch.cuda.stream(stream):
+        for it in range(warmup + steps):
+            dg.copy_(d0)
+            flush.zero_()
+            s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            _, _, _, info = bstq.stedc_leaves(dg, eg, leaf, jobz=jobz, work=work, stream=stream)
+            t.record(stream)
+            if it >= warmup:
+                times.append((s, t))
+        torch.cuda.synchronize()
+    assert int((info != 0).sum()) == 0, "unconverged leaves in the benchmark batch"
+    return statistics.mean(s.elapsed_time(t) for s, t in times)
+
+
 def time_e2e(w, steps, warmup, stream):
     """End to end through the C ABI on pinned host buffers: H2D of d and e,
     the solve, D2H of lambda, Q and info, per step."""
@@ -417,6 +446,11 @@ def main():
             workloads[f"fused syev {dtype} n={n} jobz=V batch=32768 dense N(0,1) seed 0"] = {
                 "problems_per_s": 32768 / (ms_s / 1e3), "ms": ms_s,
                 "kernel": "syev_kernel (Householder reduction + dynamic-position solve, one launch)"}
+        for dtype, n, leaf, batch in (("float32", 64, 32, 8192), ("float64", 64, 32, 8192)):
+            ms_l = time_leaves(n, leaf, batch, dtype, True, max(5, args.steps // 2), 3, flush, stream)
+            workloads[f"stedc leaves {dtype} n={n} leaf={leaf} jobz=V batch={batch} N(0,1) seed 0"] = {
+                "problems_per_s": batch / (ms_l / 1e3), "leaves_per_s": batch * (n // leaf) / (ms_l / 1e3),
+                "ms": ms_l, "kernel": "tear + batched leaf solve + gather (bstq_stedc_leaves)"}
 
     if rank != 0:
         if world > 1:

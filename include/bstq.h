@@ -228,6 +228,47 @@ size_t bstq_syev_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batc
 int bstq_syev(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const void *A,
               void *W, void *V, void *work, void *stream, const bstq_params *p);
 
+/*
+ * Leaf solve of divide and conquer (BatchLAS page "algo_steqr": the leaf
+ * solve of stedc; page "perf_steqr": steqr_cta also runs at the stedc
+ * leaves).  Each of `batch` size-n problems is cut into consecutive leaves
+ * of `leaf` rows from the top (the remainder n % leaf, if any, is a last,
+ * shorter leaf; leaf >= n gives one leaf).  At every leaf boundary r-1 | r
+ * the coupling beta = e_r is torn off as the rank-one term |beta| v v^T,
+ * v = unit_{r-1} + sign(beta) unit_r: |beta| is subtracted from the two
+ * diagonal entries next to the boundary (the upper boundary of a leaf
+ * first).  Every leaf is then solved as a steqr problem of its own (from
+ * the identity, ascending), all leaves of the batch in one batched solve
+ * (two when a shorter last leaf exists).  n >= 1, 1 <= leaf <= 64.
+ *   d     in/out  batch*n values; on exit each leaf's eigenvalues, ascending
+ *                 within the leaf, at the leaf's rows.
+ *   e     in      batch*(n-1) values (may be NULL when n == 1).
+ *   Q     out     jobz == V: the leaves' eigenvectors grouped by leaf size.
+ *                 With L = min(leaf, n), F = n / L full leaves and the last
+ *                 leaf of t = n % L rows: first batch*F blocks of L x L, block
+ *                 (b*F + k) for leaf k of problem b, then batch blocks of
+ *                 t x t, block b for problem b's last leaf; every block is
+ *                 column-major (column j the eigenvector of the leaf's j-th
+ *                 eigenvalue).  batch*(F*L*L + t*t) values in all.  Ignored
+ *                 (may be NULL) for jobz == N.
+ *   info  out     device int32[batch * leaves], leaves = F + (t > 0):
+ *                 info[b*leaves + k] is leaf k's status as for bstq_solve.
+ *                 A non-finite coupling beta poisons both leaves next to it.
+ *   work  scratch bstq_stedc_leaves_work_size(...) bytes, 256-byte aligned.
+ *   p     optional; applies to the leaf solves as in bstq_solve_ex except
+ *         back_transform, which returns -10.
+ * Returns 0; -1 dtype, -2 jobz, -3 n or leaf out of range, -4 batch, -5 d,
+ * -6 e, -7 Q, -8 info or work NULL or misaligned, -10 parameters that no
+ * leaf solve accepts; BSTQ_ERR_CUDA / BSTQ_ERR_NODEVICE as elsewhere.
+ * Like every entry point it allocates nothing and only enqueues work.
+ */
+size_t bstq_stedc_leaves_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int leaf,
+                                   int64_t batch, const bstq_params *p);
+
+int bstq_stedc_leaves(bstq_dtype dtype, bstq_jobz jobz, int n, int leaf, int64_t batch,
+                      void *d, const void *e, void *Q, int32_t *info, void *work,
+                      void *stream, const bstq_params *p);
+
 /* Description of the kernel the library would launch (for tests and
  * benchmarks): fills up to `len` bytes of `buf` with a NUL-terminated string
  * such as "lane<f32,16,V,shared,flat> tpb=224 grid=147" and returns 0, or

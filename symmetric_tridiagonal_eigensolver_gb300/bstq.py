@@ -28,7 +28,7 @@ MAX_N = 64
 EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",
            "bstq_host_work_size", "bstq_solve_host", "bstq_describe",
            "bstq_status_string", "bstq_version", "bstq_last_error", "bstq_solve_noalloc",
-           "bstq_syev_work_size", "bstq_syev")
+           "bstq_syev_work_size", "bstq_syev", "bstq_stedc_leaves_work_size", "bstq_stedc_leaves")
 
 
 class Params(ctypes.Structure):
@@ -90,6 +90,11 @@ def load(path: str = LIB_PATH):
         lib.bstq_syev_work_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P]
         lib.bstq_syev.restype = ctypes.c_int
         lib.bstq_syev.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp, vp, P]
+        lib.bstq_stedc_leaves_work_size.restype = sz
+        lib.bstq_stedc_leaves_work_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P]
+        lib.bstq_stedc_leaves.restype = ctypes.c_int
+        lib.bstq_stedc_leaves.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp,
+                                          vp, vp, vp, P]
         lib.bstq_solve_noalloc.restype = ctypes.c_int
         lib.bstq_solve_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp,
                                            vp, P]
@@ -264,3 +269,57 @@ def syev(A, jobz: bool = True, work=None, stream=None, **params):
         raise BstqError(rc, "bstq_syev")
     info = work[: 4 * batch].view(torch.int32)
     return W, (Vs.transpose(1, 2) if jobz else None), info
+
+
+def leaf_shape(n: int, leaf: int):
+    """(L, F, t): the leaf size used, the number of full leaves and the rows
+    of the shorter last leaf (0 if none), as bstq_stedc_leaves cuts a
+    size-n problem."""
+    L = min(int(leaf), int(n))
+    return L, n // L, n % L
+
+
+def stedc_leaves(d, e, leaf: int, jobz: bool = True, work=None, stream=None, **params):
+    """Leaf solve of divide and conquer on CUDA tensors: ``d`` (batch, n)
+    in/out, ``e`` (batch, n-1).  Each problem is torn into leaves of ``leaf``
+    rows (the remainder last) and every leaf solved.  Returns (d, Qf, Qt,
+    info): d holds each leaf's eigenvalues at its rows; Qf (batch, F, L, L)
+    the full leaves' eigenvectors and Qt (batch, t, t) the last shorter
+    leaf's (None if none), both with [..., :, j] the j-th eigenvector (None
+    for jobz N); info (batch, leaves) int32.  Nothing is synchronised."""
+    import torch
+    if not (d.is_cuda and d.is_contiguous() and d.dim() == 2):
+        raise ValueError("bstq.stedc_leaves: d must be a contiguous (batch, n) CUDA tensor")
+    batch, n = d.shape
+    code = _dtype_code(d.dtype)
+    L, F, t = leaf_shape(n, leaf)
+    e_ptr = None
+    if n > 1:
+        if not (e.is_cuda and e.is_contiguous() and e.dtype == d.dtype and e.numel() == batch * (n - 1)):
+            raise ValueError("bstq.stedc_leaves: e must be a contiguous CUDA tensor of d's dtype, (batch, n-1)")
+        e_ptr = e.data_ptr()
+    p = _params(**params)
+    lib = load()
+    wbytes = int(lib.bstq_stedc_leaves_work_size(code, int(bool(jobz)), int(n), int(leaf), int(batch),
+                                                 ctypes.byref(p)))
+    if wbytes == 0:
+        raise BstqError(-10, "bstq_stedc_leaves_work_size")
+    if work is None:
+        work = torch.empty(wbytes, dtype=torch.uint8, device=d.device)
+    elif work.numel() * work.element_size() < wbytes:
+        raise ValueError(f"bstq.stedc_leaves: work needs {wbytes} bytes")
+    leaves = F + (1 if t else 0)
+    info = torch.empty((batch, leaves), dtype=torch.int32, device=d.device)
+    Q = torch.empty(batch * (F * L * L + t * t), dtype=d.dtype, device=d.device) if jobz else None
+    rc = lib.bstq_stedc_leaves(code, int(bool(jobz)), int(n), int(leaf), int(batch), d.data_ptr(), e_ptr,
+                               Q.data_ptr() if jobz else None, info.data_ptr(), work.data_ptr(),
+                               _stream_handle(stream), ctypes.byref(p))
+    if rc != 0:
+        raise BstqError(rc, "bstq_stedc_leaves")
+    Qf = Qt = None
+    if jobz:
+        # library layout: column-major blocks, full leaves first, then tails
+        Qf = Q[: batch * F * L * L].view(batch, F, L, L).transpose(2, 3)
+        if t:
+            Qt = Q[batch * F * L * L:].view(batch, t, t).transpose(1, 2)
+    return d, Qf, Qt, info

@@ -10,6 +10,7 @@
 
 #include "../../include/bstq.h"
 #include "bstq_split.cuh"
+#include "bstq_leaves.h"
 #include "bstq_registry.h"
 
 namespace bstq {
@@ -550,6 +551,135 @@ extern "C" int bstq_syev(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
     cudaError_t err = cudaLaunchKernel(pl.k->fn, dim3((unsigned)pl.grid), dim3(pl.tpb), args, pl.smem,
                                        reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? 0 : cuda_fail(err, "cudaLaunchKernel");
+}
+
+// ---------------------------------------------------------------------------
+// stedc leaf solve.  Workspace: leaf diagonals of the full leaves | of the
+// tail leaves | leaf off-diagonals (full | tail) | the full leaves' solve
+// workspace | the tail leaves' solve workspace, each 256-byte aligned.
+// ---------------------------------------------------------------------------
+namespace bstq {
+namespace {
+
+struct LeafPlan {
+    int L = 0, nfull = 0, t = 0;
+    size_t off_dtail = 0, off_efull = 0, off_etail = 0, off_wfull = 0, off_wtail = 0, total = 0;
+};
+
+int make_leaf_plan(int dtype, int jobz, int n, int leaf, long long batch, const bstq_params *p, LeafPlan &lp)
+{
+    if (n < 1 || leaf < 1 || leaf > BSTQ_MAX_N)
+        return -3;
+    if (batch < 0 || (batch > 0 && (long long)n > (0x7fffffffffffffffLL / 8) / batch))
+        return -4;
+    if (p && p->back_transform)
+        return -10;  // leaves start from the identity
+    lp.L = leaf < n ? leaf : n;
+    lp.nfull = n / lp.L;
+    lp.t = n % lp.L;
+    return 0;
+}
+
+// Workspace offsets (needs the current device: the solves' plans do).
+int size_leaf_plan(int dtype, int jobz, long long batch, const bstq_params *p, LeafPlan &lp)
+{
+    const size_t elem = dtype ? 8 : 4;
+    const size_t bf = size_t(batch) * size_t(lp.nfull), bt = lp.t ? size_t(batch) : 0;
+    size_t wfull = 0, wtail = 0;
+    if (bf) {
+        int rc = check_args(dtype, jobz, lp.L, (long long)bf, p);
+        if (rc)
+            return rc;
+        wfull = bstq_work_size_ex((bstq_dtype)dtype, (bstq_jobz)jobz, lp.L, (int64_t)bf, p);
+        if (!wfull)
+            return -10;
+    }
+    if (bt) {
+        int rc = check_args(dtype, jobz, lp.t, (long long)bt, p);
+        if (rc)
+            return rc;
+        wtail = bstq_work_size_ex((bstq_dtype)dtype, (bstq_jobz)jobz, lp.t, (int64_t)bt, p);
+        if (!wtail)
+            return -10;
+    }
+    lp.off_dtail = align256(elem * bf * lp.L);
+    lp.off_efull = lp.off_dtail + align256(elem * bt * lp.t);
+    lp.off_etail = lp.off_efull + align256(elem * bf * (lp.L - 1));
+    lp.off_wfull = lp.off_etail + align256(elem * bt * (lp.t > 1 ? lp.t - 1 : 0));
+    lp.off_wtail = lp.off_wfull + align256(wfull);
+    lp.total = lp.off_wtail + align256(wtail);
+    return 0;
+}
+
+}  // namespace
+}  // namespace bstq
+
+extern "C" size_t bstq_stedc_leaves_work_size(bstq_dtype dtype, bstq_jobz jobz, int n, int leaf, int64_t batch,
+                                              const bstq_params *p)
+{
+    if (dtype != BSTQ_F32 && dtype != BSTQ_F64)
+        return 0;
+    if (jobz != BSTQ_JOBZ_N && jobz != BSTQ_JOBZ_V)
+        return 0;
+    LeafPlan lp;
+    if (make_leaf_plan(dtype, jobz, n, leaf, batch, p, lp) != 0 || size_leaf_plan(dtype, jobz, batch, p, lp) != 0)
+        return 0;
+    return lp.total > 256 ? lp.total : 256;
+}
+
+extern "C" int bstq_stedc_leaves(bstq_dtype dtype, bstq_jobz jobz, int n, int leaf, int64_t batch, void *d,
+                                 const void *e, void *Q, int32_t *info, void *work, void *stream,
+                                 const bstq_params *p)
+{
+    if (dtype != BSTQ_F32 && dtype != BSTQ_F64)
+        return -1;
+    if (jobz != BSTQ_JOBZ_N && jobz != BSTQ_JOBZ_V)
+        return -2;
+    LeafPlan lp;
+    int rc = make_leaf_plan(dtype, jobz, n, leaf, batch, p, lp);
+    if (rc)
+        return rc;
+    if (batch == 0)
+        return 0;
+    const size_t elem = dtype == BSTQ_F64 ? 8 : 4;
+    if (!d || misaligned(d, elem))
+        return -5;
+    if ((n > 1 && !e) || misaligned(e, elem))
+        return -6;
+    if (jobz == BSTQ_JOBZ_V && (!Q || misaligned(Q, elem)))
+        return -7;
+    if (!info || misaligned(info, 4) || !work || misaligned(work, 256))
+        return -8;
+    DevInfo di;
+    if (!dev_info(di))
+        return BSTQ_ERR_NODEVICE;
+    rc = size_leaf_plan(dtype, jobz, batch, p, lp);
+    if (rc)
+        return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char *w = reinterpret_cast<char *>(work);
+    char *dfull = w, *dtail = w + lp.off_dtail, *efull = w + lp.off_efull, *etail = w + lp.off_etail;
+    char *wfull = w + lp.off_wfull, *wtail = w + lp.off_wtail;
+    const int f64 = dtype == BSTQ_F64;
+    cudaError_t err = launch_leaf_tear(f64, batch, n, lp.L, d, e, dfull, efull, dtail, etail, di.sms, st);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "leaf tear");
+    const long long bf = (long long)batch * lp.nfull;
+    if (bf) {
+        rc = bstq_solve_ex(dtype, jobz, lp.L, bf, dfull, lp.L > 1 ? efull : nullptr, Q, wfull, stream, p);
+        if (rc)
+            return rc < 0 ? -10 : rc;
+    }
+    if (lp.t) {
+        char *qt = Q ? reinterpret_cast<char *>(Q) + elem * size_t(bf) * lp.L * lp.L : nullptr;
+        rc = bstq_solve_ex(dtype, jobz, lp.t, batch, dtail, lp.t > 1 ? etail : nullptr,
+                           jobz == BSTQ_JOBZ_V ? qt : nullptr, wtail, stream, p);
+        if (rc)
+            return rc < 0 ? -10 : rc;
+    }
+    err = launch_leaf_gather(f64, batch, n, lp.L, d, dfull, dtail, reinterpret_cast<const int *>(wfull),
+                             reinterpret_cast<const int *>(wtail), info, di.sms, st);
+    return err == cudaSuccess ? 0 : cuda_fail(err, "leaf gather");
 }
 
 extern "C" int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const bstq_params *p,

@@ -84,3 +84,37 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "liboracle" not in text, f
+
+
+def test_stedc_leaves_arguments(lib):
+    vp = ctypes.c_void_p
+    buf = (ctypes.c_char * 1024)()
+    good = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, vp)
+    f = lib.bstq_stedc_leaves
+    assert f(7, 1, 70, 32, 10, good, good, good, good, good, None, None) == -1
+    assert f(0, 5, 70, 32, 10, good, good, good, good, good, None, None) == -2
+    assert f(0, 1, 0, 32, 10, good, good, good, good, good, None, None) == -3
+    assert f(0, 1, 70, 0, 10, good, good, good, good, good, None, None) == -3
+    assert f(0, 1, 70, bstq.MAX_N + 1, 10, good, good, good, good, good, None, None) == -3
+    assert f(0, 1, 70, 32, -1, good, good, good, good, good, None, None) == -4
+    assert f(0, 1, 70, 32, 0, None, None, None, None, None, None, None) == 0   # batch 0: no-op
+    assert f(0, 1, 70, 32, 10, None, good, good, good, good, None, None) == -5
+    assert f(0, 1, 70, 32, 10, good, None, good, good, good, None, None) == -6
+    assert f(0, 1, 70, 32, 10, good, good, None, good, good, None, None) == -7
+    assert f(0, 1, 70, 32, 10, good, good, good, None, good, None, None) == -8
+    assert f(0, 1, 70, 32, 10, good, good, good, good, None, None, None) == -8
+    p = bstq.Params(0, 0, 0, 0, 0, 0, 1, 0)   # back_transform: leaves start from the identity
+    assert f(0, 1, 70, 32, 10, good, good, good, good, good, None, ctypes.byref(p)) == -10
+    ws = lib.bstq_stedc_leaves_work_size
+    assert ws(0, 1, 70, 0, 100, None) == 0 and ws(0, 1, 70, 32, 100, ctypes.byref(p)) == 0
+    assert bstq.leaf_shape(70, 32) == (32, 2, 6) and bstq.leaf_shape(5, 8) == (5, 1, 0)
+
+
+def test_stedc_leaves_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    vp = ctypes.c_void_p
+    buf = (ctypes.c_char * 1024)()
+    good = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, vp)
+    assert lib.bstq_stedc_leaves(0, 1, 70, 32, 10, good, good, good, good, good, None, None) == bstq.ERR_NODEVICE
