@@ -376,7 +376,8 @@ def main():
     ap.add_argument("--qstore", type=int, default=0, help="Q storage policy (with --only)")
     ap.add_argument("--kernel", type=int, default=0, help="kernel family 1 static, 2 dynamic (with --only)")
     ap.add_argument("--only", default=None,
-                    help="time one workload 'dtype:n:V|N[:batch]' and print its line (profiling aid)")
+                    help="time one workload 'dtype:n:V|N[:batch]' or 'leaves:dtype:n:leaf[:batch]' "
+                         "and print its line (profiling aid)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -410,6 +411,16 @@ def main():
     fp64_peak = sms * SM_FP64_LANES * 2 * sm_max_mhz * 1e6
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0)) * 1e9
 
+    if args.only and args.only.startswith("leaves:"):
+        # leaves:dtype:n:leaf[:batch], the stedc leaf solve alone
+        parts = args.only.split(":")
+        dtype = {"f32": "float32", "f64": "float64"}.get(parts[1], parts[1])
+        n, leaf = int(parts[2]), int(parts[3])
+        batch = int(parts[4]) if len(parts) > 4 else 8192
+        ms_l = time_leaves(n, leaf, batch, dtype, True, args.steps, args.warmup, flush, stream)
+        print(json.dumps({"workload": f"stedc leaves {dtype} n={n} leaf={leaf} jobz=V batch={batch}",
+                          "ms": ms_l, "problems_per_s": batch / (ms_l / 1e3)}))
+        return 0
     if args.only:
         parts = args.only.split(":")
         w = dict(dtype={"f32": "float32", "f64": "float64"}.get(parts[0], parts[0]), n=int(parts[1]),
