@@ -45,27 +45,39 @@ COMPANIONS = [dict(dtype="float32", n=8, batch=65536, jobz=True),
 # (BatchLAS perf_steqr, "What ships" table: 450.9 us per call).
 PAGES_BASELINE = 32768 / 450.9e-6
 # DRAM bytes (read + write) per launch measured by ncu for a kernel variant,
-# keyed by bstq_describe()'s text and the digest of the CUDA sources
+# keyed by bstq_describe()'s text and the digest of the kernel's sources
 # (kernel_digest()); a changed kernel no longer matches and reports null
 # (profiles/split_f32_n16_V_batch32768.md).
 NCU_TRAFFIC = {
-    ("lane<f32,16,V,split,flat> tpb=512 grid=152 smem=207984 regs=128 work=131072", "52a19c0d673a751e"):
-        4.303616e6 + 0.212224e6,
+    ("lane<f32,16,V,split,flat> tpb=512 grid=152 smem=207984 regs=128 work=131072", "7cd0d4d9ea0290f2"):
+        4.312320e6 + 0.149504e6,
 }
 
 
-def kernel_digest() -> str:
-    """Short SHA-256 over the library's CUDA sources (csrc/*.cu, *.cuh, *.h,
-    *.inc) and its header, in name order."""
+# Translation unit of the headline kernel (split roles, float, n <= 16, V).
+HEADLINE_UNIT = "bstq_kern_split_f32_v16.cu"
+
+
+def kernel_digest(unit: str = HEADLINE_UNIT) -> str:
+    """Short SHA-256 over the CUDA sources the kernel's translation unit
+    compiles: the unit and every header it includes with quotes, followed
+    recursively, in name order.  Launch shape, registers and shared memory
+    are in bstq_describe()'s text, the other half of the traffic key."""
     import hashlib
-    pkg = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300")
-    files = sorted(os.path.join(pkg, "csrc", f) for f in os.listdir(os.path.join(pkg, "csrc"))
-                   if f.endswith((".cu", ".cuh", ".h", ".inc")))
-    files.append(os.path.join(ROOT, "include", "bstq.h"))
+    import re
+    csrc = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300", "csrc")
+    seen, todo = set(), [unit]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo.extend(re.findall(r'^\s*#\s*include\s+"([^"]+)"', fh.read(), flags=re.M))
     h = hashlib.sha256()
-    for f in files:
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for f in sorted(seen):
+        h.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

@@ -35,21 +35,25 @@ struct LeafShape {
     int n, L, nfull, t;
 };
 
-template <typename T>
+// Row g of the batch -> (problem b, row i).  I is the index type: 32-bit
+// unsigned where batch * n fits (its division is a short sequence; the
+// 64-bit one is a long software routine that dominated these kernels).
+template <typename T, typename I>
 __global__ void tear_kernel(LeafShape s, const T *__restrict__ d, const T *__restrict__ e, T *__restrict__ dfull,
                             T *__restrict__ efull, T *__restrict__ dtail, T *__restrict__ etail)
 {
-    const long long total = s.batch * s.n;
-    const long long step = (long long)gridDim.x * blockDim.x;
-    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += step) {
-        const long long b = g / s.n;
-        const int i = (int)(g - b * s.n);
+    const I total = (I)(s.batch * s.n);
+    const I step = (I)gridDim.x * blockDim.x;
+    const I nn = (I)s.n;
+    for (I g = (I)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += step) {
+        const long long b = (long long)(g / nn);
+        const int i = (int)(g - (I)b * nn);
         const int k = i / s.L;
         const int j = i - k * s.L;
         const bool full = k < s.nfull;
         const int nk = full ? s.L : s.t;
         const T *eb = e + b * (s.n - 1);
-        T x = d[g];
+        T x = d[(long long)g];
         if (j == 0 && i > 0)
             x = x - absv(eb[i - 1]);
         if (j == nk - 1 && i < s.n - 1)
@@ -67,26 +71,27 @@ __global__ void tear_kernel(LeafShape s, const T *__restrict__ d, const T *__res
     }
 }
 
-template <typename T>
+template <typename T, typename I>
 __global__ void gather_kernel(LeafShape s, T *__restrict__ d, const T *__restrict__ dfull,
                               const T *__restrict__ dtail, const int *__restrict__ info_full,
                               const int *__restrict__ info_tail, int *__restrict__ info)
 {
-    const long long total = s.batch * s.n;
-    const long long step = (long long)gridDim.x * blockDim.x;
+    const I total = (I)(s.batch * s.n);
+    const I step = (I)gridDim.x * blockDim.x;
+    const I nn = (I)s.n;
     const int leaves = s.nfull + (s.t > 0 ? 1 : 0);
-    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += step) {
-        const long long b = g / s.n;
-        const int i = (int)(g - b * s.n);
+    for (I g = (I)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += step) {
+        const long long b = (long long)(g / nn);
+        const int i = (int)(g - (I)b * nn);
         const int k = i / s.L;
         const int j = i - k * s.L;
         if (k < s.nfull) {
             const long long leaf = b * s.nfull + k;
-            d[g] = dfull[leaf * s.L + j];
+            d[(long long)g] = dfull[leaf * s.L + j];
             if (j == 0)
                 info[b * leaves + k] = info_full[leaf];
         } else {
-            d[g] = dtail[b * s.t + j];
+            d[(long long)g] = dtail[b * s.t + j];
             if (j == 0)
                 info[b * leaves + k] = info_tail[b];
         }
@@ -94,6 +99,12 @@ __global__ void gather_kernel(LeafShape s, T *__restrict__ d, const T *__restric
 }
 
 constexpr int kLeafThreads = 256;
+
+// 32-bit indexing needs total rows plus one grid stride below 2^32.
+bool fits32(long long total, long long grid)
+{
+    return total + grid * kLeafThreads < (1LL << 32);
+}
 
 long long leaf_grid(long long total, int sms)
 {
@@ -112,12 +123,21 @@ cudaError_t launch_leaf_tear(int f64, long long batch, int n, int L, const void 
     const long long grid = leaf_grid(batch * n, sms);
     if (grid <= 0)
         return cudaSuccess;
-    if (f64)
-        tear_kernel<double><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+    const bool w32 = fits32(batch * n, grid);
+    if (f64 && w32)
+        tear_kernel<double, unsigned><<<(unsigned)grid, kLeafThreads, 0, st>>>(
             s, (const double *)d, (const double *)e, (double *)dfull, (double *)efull, (double *)dtail,
             (double *)etail);
+    else if (f64)
+        tear_kernel<double, unsigned long long><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+            s, (const double *)d, (const double *)e, (double *)dfull, (double *)efull, (double *)dtail,
+            (double *)etail);
+    else if (w32)
+        tear_kernel<float, unsigned><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+            s, (const float *)d, (const float *)e, (float *)dfull, (float *)efull, (float *)dtail,
+            (float *)etail);
     else
-        tear_kernel<float><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+        tear_kernel<float, unsigned long long><<<(unsigned)grid, kLeafThreads, 0, st>>>(
             s, (const float *)d, (const float *)e, (float *)dfull, (float *)efull, (float *)dtail,
             (float *)etail);
     return cudaGetLastError();
@@ -131,11 +151,18 @@ cudaError_t launch_leaf_gather(int f64, long long batch, int n, int L, void *d, 
     const long long grid = leaf_grid(batch * n, sms);
     if (grid <= 0)
         return cudaSuccess;
-    if (f64)
-        gather_kernel<double><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+    const bool w32 = fits32(batch * n, grid);
+    if (f64 && w32)
+        gather_kernel<double, unsigned><<<(unsigned)grid, kLeafThreads, 0, st>>>(
             s, (double *)d, (const double *)dfull, (const double *)dtail, info_full, info_tail, info);
+    else if (f64)
+        gather_kernel<double, unsigned long long><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+            s, (double *)d, (const double *)dfull, (const double *)dtail, info_full, info_tail, info);
+    else if (w32)
+        gather_kernel<float, unsigned><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+            s, (float *)d, (const float *)dfull, (const float *)dtail, info_full, info_tail, info);
     else
-        gather_kernel<float><<<(unsigned)grid, kLeafThreads, 0, st>>>(
+        gather_kernel<float, unsigned long long><<<(unsigned)grid, kLeafThreads, 0, st>>>(
             s, (float *)d, (const float *)dfull, (const float *)dtail, info_full, info_tail, info);
     return cudaGetLastError();
 }
