@@ -469,6 +469,15 @@ def main():
             workloads[f"fused syev {dtype} n={n} jobz=V batch=32768 dense N(0,1) seed 0"] = {
                 "problems_per_s": 32768 / (ms_s / 1e3), "ms": ms_s,
                 "kernel": "syev_kernel (Householder reduction + dynamic-position solve, one launch)"}
+        # saturation knee: per-problem time at 4x the batch against the batch
+        for w in (HEADLINE, COMPANIONS[3]):
+            w4 = dict(w, batch=4 * w["batch"])
+            m4, _, _, desc4 = time_workload(w4, max(5, args.steps // 2), 3, lambda: None, flush, stream)
+            t1 = statistics.mean(ms) / 1e3 if w is HEADLINE else workloads[wl_name(w)]["ms"] / 1e3
+            t4 = statistics.mean(m4) / 1e3
+            workloads[f"saturation: {wl_name(w4)}"] = {
+                "problems_per_s": w4["batch"] / t4, "ms": t4 * 1e3, "kernel": desc4,
+                "per_problem_time_vs_batch": (t4 / w4["batch"]) / (t1 / w["batch"])}
         for dtype, n, leaf, batch in (("float32", 64, 32, 8192), ("float64", 64, 32, 8192)):
             ms_l = time_leaves(n, leaf, batch, dtype, True, max(5, args.steps // 2), 3, flush, stream)
             workloads[f"stedc leaves {dtype} n={n} leaf={leaf} jobz=V batch={batch} N(0,1) seed 0"] = {
