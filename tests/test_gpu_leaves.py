@@ -134,3 +134,49 @@ def test_work_size_covers_both_solves():
     w = lib.bstq_stedc_leaves_work_size(0, 1, 70, 32, 100, None)
     assert w >= 4 * (100 * 70 + 100 * 67) + lib.bstq_work_size(0, 1, 32, 200) + lib.bstq_work_size(0, 1, 6, 100)
     assert lib.bstq_stedc_leaves_work_size(1, 0, 64, 32, 8192, None) > 0
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_nested_scheduler_equals_flat(dt):
+    d, e = inputs.normal_problems(40, 900, dt, seed=13)
+    a = run_leaves(d, e, 16, scheduler=1)
+    b = run_leaves(d, e, 16, scheduler=2)
+    for x, y in zip(a, b):
+        assert (x is None and y is None) or np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_unsorted_and_pg_leaves(dt):
+    """no_sort leaves each leaf's spectrum unsorted (same values as the sorted
+    call within the bound); the PG update scheme meets the same bounds."""
+    n, leaf = 50, 16
+    d, e = inputs.normal_problems(n, 700, dt, seed=17)
+    ref = oracle.stedc_leaves(d, e, leaf, jobz=True, nthreads=ORACLE_THREADS)
+    lam_u, Qf_u, Qt_u, info_u = run_leaves(d, e, leaf, no_sort=True)
+    assert np.array_equal(info_u, ref.info)
+    for k, (s, m) in enumerate(zip(ref.starts, ref.sizes)):
+        dl, el = ref.d_torn[:, s:s + m], e[:, s:s + m - 1]
+        got = np.sort(lam_u[:, s:s + m], axis=1)
+        lref = _LeafRef(ref.lam[:, s:s + m], None, ref.info[:, k])
+        check_parity(dl, el, got, None, info_u[:, k], lref, what=f"no_sort leaf {k}")
+    _check(d, e, leaf, update_scheme="pg")
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_exhausted_budget_matches_the_oracle_status(dt):
+    d, e = inputs.normal_problems(32, 600, dt, seed=19)
+    ref = oracle.stedc_leaves(d, e, 16, jobz=True, maxit_per_n=1, nthreads=ORACLE_THREADS)
+    lam, Qf, Qt, info = run_leaves(d, e, 16, max_sweeps_per_n=1)
+    assert np.any(ref.info > 0)
+    # the count of unconverged off-diagonals matches the oracle up to the
+    # rounding of deflation decisions
+    assert np.mean(info == ref.info) > 0.9 and np.mean((info > 0) == (ref.info > 0)) > 0.95
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_degenerate_sizes(dt):
+    # one row per problem; one problem; leaf size equal to n
+    for n, leaf, batch in ((1, 1, 50), (1, 32, 7), (33, 33, 1), (2, 1, 300), (64, 64, 200)):
+        d, e = inputs.normal_problems(n, batch, dt, seed=n + batch)
+        _check(d, e, leaf, jobz=True)
+        _check(d, e, leaf, jobz=False)
