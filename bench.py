@@ -58,12 +58,10 @@ NCU_TRAFFIC = {
 HEADLINE_UNIT = "bstq_kern_split_f32_v16.cu"
 
 
-def kernel_digest(unit: str = HEADLINE_UNIT) -> str:
-    """Short SHA-256 over the CUDA sources the kernel's translation unit
-    compiles: the unit and every header it includes with quotes, followed
-    recursively, in name order.  Launch shape, registers and shared memory
-    are in bstq_describe()'s text, the other half of the traffic key."""
-    import hashlib
+def kernel_sources(unit: str = HEADLINE_UNIT) -> list:
+    """The CUDA sources a kernel's translation unit compiles: the unit and
+    every header it includes with quotes, followed recursively; names in
+    order."""
     import re
     csrc = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300", "csrc")
     seen, todo = set(), [unit]
@@ -74,8 +72,17 @@ def kernel_digest(unit: str = HEADLINE_UNIT) -> str:
         seen.add(f)
         with open(os.path.join(csrc, f)) as fh:
             todo.extend(re.findall(r'^\s*#\s*include\s+"([^"]+)"', fh.read(), flags=re.M))
+    return sorted(seen)
+
+
+def kernel_digest(unit: str = HEADLINE_UNIT) -> str:
+    """Short SHA-256 over kernel_sources(unit), names and contents.  Launch
+    shape, registers and shared memory are in bstq_describe()'s text, the
+    other half of the traffic key."""
+    import hashlib
+    csrc = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(seen):
+    for f in kernel_sources(unit):
         h.update(f.encode())
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
@@ -273,8 +280,7 @@ def time_leaves(n, leaf, batch, dtype, jobz, steps, warmup, flush, stream):
     d0 = torch.from_numpy(d).cuda()
     dg = torch.empty_like(d0)
     eg = torch.from_numpy(e).cuda()
-    work = torch.empty(int(bstq.load().bstq_stedc_leaves_work_size(bstq._dtype_code(dt), int(jobz), n, leaf, batch,
-                                                                   None)), dtype=torch.uint8, device="cuda")
+    work = torch.empty(bstq.stedc_leaves_work_size(dt, jobz, n, leaf, batch), dtype=torch.uint8, device="cuda")
     times = []
     with torch.cuda.stream(stream):
         for it in range(warmup + steps):

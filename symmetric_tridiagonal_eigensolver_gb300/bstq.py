@@ -279,6 +279,12 @@ def leaf_shape(n: int, leaf: int):
     return L, n // L, n % L
 
 
+def stedc_leaves_work_size(dtype, jobz: bool, n: int, leaf: int, batch: int, **params) -> int:
+    p = _params(**params)
+    return int(load().bstq_stedc_leaves_work_size(_dtype_code(dtype), int(bool(jobz)), int(n), int(leaf),
+                                                  int(batch), ctypes.byref(p)))
+
+
 def stedc_leaves(d, e, leaf: int, jobz: bool = True, work=None, stream=None, **params):
     """Leaf solve of divide and conquer on CUDA tensors: ``d`` (batch, n)
     in/out, ``e`` (batch, n-1).  Each problem is torn into leaves of ``leaf``
