@@ -13,8 +13,8 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests are skipped, not failed, where no GPU is visible; the driver
-    # selects them with -m gpu on the GPU machine.
+    # GPU tests are skipped, not failed, where no GPU is visible; run them
+    # with -m gpu on a machine with a GB300.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
