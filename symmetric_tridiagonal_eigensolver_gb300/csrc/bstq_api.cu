@@ -727,7 +727,7 @@ extern "C" const char *bstq_status_string(int code)
     case -1: return "invalid dtype";
     case -2: return "invalid jobz";
     case -3: return "n outside [1, 64]";
-    case -4: return "invalid batch";
+    case -4: return "invalid batch (bstq_solve_noalloc: more problems than its fixed scratch array holds)";
     case -5: return "d is NULL or misaligned";
     case -6: return "e is NULL or misaligned";
     case -7: return "Q is NULL or misaligned";

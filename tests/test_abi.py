@@ -38,6 +38,8 @@ def test_version_and_status_strings(lib):
     assert bstq.version().startswith("bstq")
     assert bstq.status_string(0) == "success"
     assert "n outside" in bstq.status_string(-3)
+    # the allocation-free entry point's size limit is named in the text of -4
+    assert "fixed scratch" in bstq.status_string(-4)
 
 
 def test_invalid_arguments_are_rejected_before_any_device_use(lib):
