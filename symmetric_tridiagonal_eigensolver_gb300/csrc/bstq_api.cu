@@ -11,6 +11,7 @@
 #include "../../include/bstq.h"
 #include "bstq_split.cuh"
 #include "bstq_leaves.h"
+#include "bstq_plan.h"
 #include "bstq_registry.h"
 
 namespace bstq {
@@ -275,28 +276,13 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         tpb = p->threads_per_block;
         if (tpb > cap)
             return -10;
-    } else if (batch <= (long long)di.sms * cap || dtype == BSTQ_F64) {
-        // W waves of one block per SM, the fewest a block of at most `cap`
-        // threads allows, with the problems spread evenly over the blocks:
-        // one wave when the whole batch fits.  Beyond one wave only for
-        // double, whose kernels the FP64 pipe bounds, so an even load per SM
-        // and wave pays (at n = 12 V, batch 131072, 128-thread blocks left a
-        // quarter-full last wave and took 1.18x the per-problem time of
-        // batch 32768, these blocks 0.98x).
-        const long long per_wave = (long long)di.sms * cap;
-        const long long waves = batch > 0 ? (batch + per_wave - 1) / per_wave : 1;
-        const long long want = (batch + di.sms * waves - 1) / (di.sms * waves);
-        tpb = (int)((want + 31) / 32 * 32);
-        if (tpb < 32)
-            tpb = 32;
-        if (tpb > cap)
-            tpb = cap;
     } else {
-        // float beyond one wave: 128-thread blocks, several per SM.  These
-        // kernels are bound by their dependency chains; a full first wave
-        // and a short last one measured slightly faster than even waves of
-        // one block per SM at n = 8 V, batch 65536 (0.057 vs 0.059 ms).
-        tpb = cap < 128 ? cap : 128;
+        // bstq_plan.h: one wave of one block per SM when the batch fits;
+        // beyond, even waves for double (at n = 12 V, batch 131072,
+        // 128-thread blocks left a quarter-full last wave and took 1.18x the
+        // per-problem time of batch 32768, even waves 0.98x), 128-thread
+        // blocks for float (n = 8 V, batch 65536: 0.057 against 0.059 ms)
+        tpb = choose_block_size(batch, di.sms, cap, dtype == BSTQ_F64);
     }
     pl.tpb = tpb;
     pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
