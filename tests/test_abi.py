@@ -120,3 +120,14 @@ def test_stedc_leaves_reports_no_device(lib):
     buf = (ctypes.c_char * 1024)()
     good = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, vp)
     assert lib.bstq_stedc_leaves(0, 1, 70, 32, 10, good, good, good, good, good, None, None) == bstq.ERR_NODEVICE
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libbstq.so the binding raises: there is no CPU fallback."""
+    import subprocess
+    import sys
+    code = ("from symmetric_tridiagonal_eigensolver_gb300 import bstq\n"
+            f"bstq.load({str(tmp_path / 'libbstq.so')!r})\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libbstq.so not found" in r.stderr
