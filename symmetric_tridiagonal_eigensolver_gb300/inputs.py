@@ -50,11 +50,14 @@ def class_counts(batch: int):
     return counts
 
 
-def mixed_problems(n: int, batch: int, dtype, seed: int = 0):
+def mixed_problems(n: int, batch: int, dtype, seed: int = 0, big: float = 1e18, tiny: float = 1e-18):
     """Mixed hard-case batch.  Returns d, e (rounded to dtype), the class label
     of each problem (int8, index into MIXED_CLASSES) and the Toeplitz (a, b)
     pair of each problem (float64 before rounding; meaningful only for the
-    'toeplitz' class, whose stored d and e are a and b rounded to dtype)."""
+    'toeplitz' class, whose stored d and e are a and b rounded to dtype).
+    ``big`` and ``tiny`` are the factors of the 'big' and 'tiny' classes
+    (1e+18 and 1e-18 as the workload states; other values, e.g. powers of two
+    beyond float64's scaling thresholds, give the same draws rescaled)."""
     dt = _as_dtype(dtype)
     rng = np.random.default_rng(seed)
     d = rng.standard_normal((batch, n))
@@ -81,16 +84,67 @@ def mixed_problems(n: int, batch: int, dtype, seed: int = 0):
     e[z] = 0.0
 
     b = labels == CLASS_INDEX["big"]
-    d[b] *= 1e18
-    e[b] *= 1e18
+    d[b] *= big
+    e[b] *= big
     t = labels == CLASS_INDEX["tiny"]
-    d[t] *= 1e-18
-    e[t] *= 1e-18
+    d[t] *= tiny
+    e[t] *= tiny
 
     tp = labels == CLASS_INDEX["toeplitz"]
     d[tp] = ab[tp, 0:1]
     e[tp] = ab[tp, 1:2]
     return d.astype(dt), e.astype(dt), labels, ab
+
+
+# Exponents k of the scaled-extremes inputs (N(0,1) problems times 2^k), per
+# precision: unscaled, above the down-scaling threshold ssfmax (twice, the
+# second close to overflow), below the up-scaling threshold ssfmin, low
+# enough that squared entries fall under the smallest normal number, and two
+# with a subnormal block norm (the second, in float32, so deep that
+# ssfmin / norm would overflow without the exact power-of-two lift).
+SCALE_EXPONENTS = {
+    np.dtype(np.float32): (0, 64, 120, -70, -100, -140, -146),
+    np.dtype(np.float64): (0, 520, 1000, -420, -530, -1060),
+}
+
+
+def scaled_problems(n: int, batch: int, dtype, seed: int = 0, exponents=None):
+    """N(0,1) problems, problem b multiplied by 2^k_b with k_b taken in turn
+    from ``exponents`` (default SCALE_EXPONENTS of the dtype).  The product is
+    formed exactly in float64 (np.ldexp) and rounded to dtype last, so
+    subnormal results are the correctly rounded values.  Returns d, e and k
+    (int32, per problem)."""
+    dt = _as_dtype(dtype)
+    exps = np.asarray(SCALE_EXPONENTS[dt] if exponents is None else exponents, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((batch, n))
+    e = rng.standard_normal((batch, max(n - 1, 0)))
+    k = exps[np.arange(batch) % len(exps)]
+    d = np.ldexp(d, k[:, None])
+    e = np.ldexp(e, k[:, None])
+    return d.astype(dt), e.astype(dt), k
+
+
+def block_scaled_problems(n: int, batch: int, dtype, seed: int = 0, exponents=None):
+    """Two blocks per problem with different scales: N(0,1) d and e, the
+    off-diagonal at a random row r (1 <= r <= n-1) set to zero, rows [0, r)
+    multiplied by 2^k1 and rows [r, n) by 2^k2, k1 and k2 drawn from
+    ``exponents`` (default SCALE_EXPONENTS of the dtype).  n >= 2.  Returns
+    d, e, r, k1, k2."""
+    dt = _as_dtype(dtype)
+    exps = np.asarray(SCALE_EXPONENTS[dt] if exponents is None else exponents, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((batch, n))
+    e = rng.standard_normal((batch, n - 1))
+    r = rng.integers(1, n, size=batch)
+    k1 = exps[rng.integers(0, len(exps), size=batch)]
+    k2 = exps[rng.integers(0, len(exps), size=batch)]
+    rows = np.arange(n)[None, :]
+    kd = np.where(rows < r[:, None], k1[:, None], k2[:, None])
+    e[np.arange(batch), r - 1] = 0.0
+    d = np.ldexp(d, kd)
+    e = np.ldexp(e, kd[:, : n - 1])
+    return d.astype(dt), e.astype(dt), r, k1, k2
 
 
 def problems(kind: str, n: int, batch: int, dtype, seed: int = 0):

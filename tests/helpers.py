@@ -11,6 +11,12 @@ def eps_of(dtype) -> float:
     return EPS[np.dtype(dtype)]
 
 
+def tiny_of(dtype) -> float:
+    """Smallest positive subnormal of the dtype: the spacing of the grid a
+    result with a subnormal magnitude is rounded to."""
+    return float(np.finfo(dtype).smallest_subnormal)
+
+
 def dense(d, e, dtype=np.float64):
     """Dense (batch, n, n) symmetric tridiagonal matrices."""
     d = np.asarray(d, dtype=dtype)
@@ -44,6 +50,33 @@ def norm1(d, e):
 def lam_tol(n, dtype, tnorm):
     """|lambda - lambda_ref| <= 16 n eps ||T||."""
     return 16.0 * n * eps_of(dtype) * np.asarray(tnorm, dtype=np.float64)
+
+
+def lam_tol_sub(n, dtype, tnorm):
+    """16 n eps ||T|| plus one subnormal spacing: where ||T|| is itself near or
+    below the smallest normal number, every eigenvalue is rounded to the
+    subnormal grid when it is scaled back, so two correct results can differ
+    by that spacing however small 16 n eps ||T|| is.  For normal ||T|| the
+    extra term is negligible.  Returned in long double, so that tolerances
+    far below the dtype's own range stay exact."""
+    return (np.longdouble(16.0 * n * eps_of(dtype)) * np.asarray(tnorm, dtype=np.longdouble)
+            + np.longdouble(tiny_of(dtype)))
+
+
+def tri_residual_ld(d, e, lam, Q):
+    """max |T Q - Q Lambda| per problem from the band structure, in long
+    double (exact products of subnormal entries, no overflow near the top of
+    float64's range)."""
+    ld = np.longdouble
+    d = np.asarray(d, dtype=ld)
+    e = np.asarray(e, dtype=ld).reshape(len(d), max(d.shape[1] - 1, 0))
+    Qd = np.asarray(Q, dtype=ld)
+    TQ = d[:, :, None] * Qd
+    if d.shape[1] > 1:
+        TQ[:, 1:, :] += e[:, :, None] * Qd[:, :-1, :]
+        TQ[:, :-1, :] += e[:, :, None] * Qd[:, 1:, :]
+    R = TQ - Qd * np.asarray(lam, dtype=ld)[:, None, :]
+    return np.abs(R).reshape(len(d), -1).max(1)
 
 
 def residual_orth(d, e, lam, Q):

@@ -15,8 +15,10 @@ from tests import helpers as H
 
 ORACLE_DIR = os.path.dirname(os.path.abspath(oracle.__file__))
 IMPL = "steqr_oracle_impl.h"
+CONSTS = "steqr_oracle.c"
 
-# (name, exact source text, replacement)
+# (name, exact source text, replacement) in the generic body; entries of
+# four are (name, file, exact source text, replacement)
 MUTATIONS = [
     ("exp_sign_2csb", "DD(i0) = c * c * aa + (real_t)2 * c * s * bb + s * s * cc;",
      "DD(i0) = c * c * aa - (real_t)2 * c * s * bb + s * s * cc;"),
@@ -52,6 +54,15 @@ MUTATIONS = [
      "real_t beta = R_COPYSIGN(FN(hypot2)(alpha, xnorm), alpha);"),
     ("sytd2_q_forward_order", "for (int i = n - 2; i >= 0; --i) {\n            if (tau[i] == (real_t)0)",
      "for (int i = 0; i <= n - 2; ++i) {\n            if (tau[i] == (real_t)0)"),
+    # scaling (algo_steqr, the scaling paragraph): thresholds, the exact
+    # lift of a subnormal norm, and the scale-back
+    ("f64_ssfmax_never_scales", CONSTS, "#define R_SSFMAX (0x1p511 / 3.0)", "#define R_SSFMAX (0x1p1023)"),
+    ("f64_ssfmin_never_scales", CONSTS, "#define R_SSFMIN 0x1p-405", "#define R_SSFMIN 0x1p-1020"),
+    ("f32_ssfmax_never_scales", CONSTS, "#define R_SSFMAX (0x1p63f / 3.0f)", "#define R_SSFMAX (0x1p127f)"),
+    ("f32_prescale_dropped", CONSTS, "#define R_PRESCALE_F32 16777216.0f", "#define R_PRESCALE_F32 1.0f"),
+    ("prescale_not_undone", "real_t upre = (real_t)1 / pre;", "real_t upre = (real_t)1;"),
+    ("prescale_skips_e", "e[i] = (e[i] * pre) * sc;", "e[i] = e[i] * sc;"),
+    ("unscale_down_inverted", "real_t us = anorm / R_SSFMAX;", "real_t us = R_SSFMAX / anorm;"),
 ]
 
 
@@ -99,6 +110,17 @@ def pin_failures(lib):
             ref = np.linalg.eigvalsh(H.dense(ds, es))
             lam = np.nan_to_num(r.lam.astype(np.float64), nan=1e300)
             check(f"scaled{fac}", np.all(np.abs(lam - ref).max(1) <= H.lam_tol(8, dt, tn)))
+        # scaled extremes: N(0,1) times 2^k across every scaling branch,
+        # against 2^k times the library spectrum of the exactly rescaled
+        # matrix
+        d, e, k = inputs.scaled_problems(8, 4 * len(inputs.SCALE_EXPONENTS[np.dtype(dt)]), dt, seed=90)
+        r = oracle.steqr(d, e, jobz=True, lib=lib)
+        check("scaled_info", np.all(r.info == 0))
+        dr = np.ldexp(d.astype(np.float64), -k[:, None])
+        er = np.ldexp(e.astype(np.float64), -k[:, None])
+        ref = np.ldexp(np.linalg.eigvalsh(H.dense(dr, er)).astype(np.longdouble), k[:, None])
+        lam = np.nan_to_num(r.lam.astype(np.longdouble), nan=np.longdouble(1e300))
+        check("scaled_lam", np.all(np.abs(lam - ref).max(1) <= H.lam_tol_sub(8, dt, H.norm1(d, e))))
         # pre-split: every eigenvector on one block
         d, e = inputs.normal_problems(9, 10, dt, seed=4)
         e[:, 3] = 0
@@ -177,15 +199,15 @@ def build_dir(tmp_path_factory):
     return tmp_path_factory.mktemp("oracle_mutants")
 
 
-def _build_variant(build_dir, name, old, new):
+def _build_variant(build_dir, name, old, new, fname=IMPL):
     src = build_dir / name
     src.mkdir()
     for f in oracle._SOURCES:
         shutil.copy(os.path.join(ORACLE_DIR, f), src / f)
     if old is not None:
-        text = (src / IMPL).read_text()
+        text = (src / fname).read_text()
         assert text.count(old) == 1, f"mutation anchor not unique: {name}"
-        (src / IMPL).write_text(text.replace(old, new))
+        (src / fname).write_text(text.replace(old, new))
     out = oracle.build(force=True, src_dir=str(src), out_path=str(src / "lib.so"))
     return oracle.load_variant(out)
 
@@ -195,7 +217,11 @@ def test_unmodified_oracle_passes_compact_pins(build_dir):
     assert pin_failures(lib) == []
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(build_dir, name, old, new):
-    lib = _build_variant(build_dir, name, old, new)
+def _spec(m):
+    return (m[0], IMPL, m[1], m[2]) if len(m) == 3 else m
+
+
+@pytest.mark.parametrize("name,fname,old,new", [_spec(m) for m in MUTATIONS], ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(build_dir, name, fname, old, new):
+    lib = _build_variant(build_dir, name, old, new, fname)
     assert pin_failures(lib) != [], f"mutation {name} slipped through every pin"
