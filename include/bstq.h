@@ -193,6 +193,11 @@ int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
  * float problems of n <= 32); other codes as bstq_solve_ex.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * The address is kept per device ordinal for the rest of the process: it
+ * belongs to the device's primary context, the one the CUDA runtime uses.
+ * A caller that makes another context current on the device, or resets the
+ * device (cudaDeviceReset) after the first call, must not call this entry
+ * point afterwards.
  * All calls share the one array and the kernel overwrites the part it uses
  * before reading it, so nothing needs clearing between calls; calls that can
  * overlap on the GPU (different streams, or graphs replayed concurrently)
@@ -275,6 +280,63 @@ int bstq_stedc_leaves(bstq_dtype dtype, bstq_jobz jobz, int n, int leaf, int64_t
  * returns -k for invalid arguments as bstq_solve_ex would. */
 int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
                   const bstq_params *p, char *buf, size_t len);
+
+/*
+ * Diagnostics: one building block of the solve, run on a table of inputs so
+ * that it can be checked on its own (the tests' unit layer).  Each op calls
+ * the same device code the solver kernels run.  The BatchLAS pages define
+ * the blocks (page "algo_steqr": Givens rotation, copysign shift, 2x2 solve,
+ * EXP and PG update schemes, eigenvector accumulation); this entry point
+ * itself has no counterpart there.
+ *
+ * `in` and `out` are device arrays of the dtype; `count` records are
+ * processed, record k at in + k * (values in) and out + k * (values out):
+ *   RCP, SQRT, RSQRT, HYP1  1 -> 1   1/x, sqrt x, 1/sqrt x (x normal, > 0),
+ *                                    sqrt(1 + x^2)
+ *   DIV                     2 -> 1   a / b (b normal)
+ *   LARTG                   2 -> 3   (f, g) -> (c, s, r), G^T [f; g] = [r; 0]
+ *   LARTG_FAST (f64 only)   2 -> 3   the chase's fast double form
+ *   SHIFT                   3 -> 4   (d1, d2, e1) -> (t, mu, cs, sn): the 2x2
+ *                                    tangent, the copysign shift and the 2x2
+ *                                    rotation of the leading block
+ *   PASS_STATIC, PASS_DYN_EXP, PASS_DYN_PG    42 -> 288
+ *       one pass of the chase at compile-time size 16 in the static- or
+ *       dynamic-position family.  Record: n, lo, m, task (1 sweep over
+ *       positions m .. lo+1, 2 the 2x2 solve at lo+1), rhi, rlo (the warp's
+ *       union of positions, containing [lo+1, m]), f0, g0 (the sweep's
+ *       seed: d_m - mu, e_{m-1}), cs2, sn2 (the 2x2 rotation), d[16], e[16]
+ *       (integers stored as values of the dtype).  Result: d[16], e[16]
+ *       after the pass, then the 16 x 16 column-major product of the pass's
+ *       rotations Q, so that T_after = Q^T T_before Q.
+ *   FASTQ (f64 only)        30 K -> 256
+ *       the factored double eigenvector update alone: K = arg sweeps over
+ *       positions 15 .. 1 of a 16 x 16 Q starting at the identity, the
+ *       rotation (c, s) of sweep k, step j at values (k * 15 + j) * 2.
+ *       Result: Q, column-major.
+ * `work` (device, 16-byte aligned) holds bstq_diag_work_size(...) bytes for
+ * PASS_DYN_* and FASTQ and may be NULL otherwise.  Returns 0; -1 unknown op
+ * for the dtype, -2 dtype, -3 count, -4 arg, -5 in, -6 out, -7 work;
+ * BSTQ_ERR_CUDA / BSTQ_ERR_NODEVICE as elsewhere.  Allocates nothing.
+ */
+typedef enum {
+    BSTQ_DIAG_RCP = 1,
+    BSTQ_DIAG_DIV = 2,
+    BSTQ_DIAG_SQRT = 3,
+    BSTQ_DIAG_RSQRT = 4,
+    BSTQ_DIAG_HYP1 = 5,
+    BSTQ_DIAG_LARTG = 6,
+    BSTQ_DIAG_LARTG_FAST = 7,
+    BSTQ_DIAG_SHIFT = 8,
+    BSTQ_DIAG_PASS_STATIC = 20,
+    BSTQ_DIAG_PASS_DYN_EXP = 21,
+    BSTQ_DIAG_PASS_DYN_PG = 22,
+    BSTQ_DIAG_FASTQ = 30
+} bstq_diag_op;
+
+size_t bstq_diag_work_size(int op, bstq_dtype dtype, int64_t count);
+
+int bstq_diag(int op, bstq_dtype dtype, int64_t count, int arg, const void *in, void *out, void *work,
+              void *stream);
 
 /* Human-readable text for a return code. */
 const char *bstq_status_string(int code);

@@ -28,7 +28,18 @@ MAX_N = 64
 EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",
            "bstq_host_work_size", "bstq_solve_host", "bstq_describe",
            "bstq_status_string", "bstq_version", "bstq_last_error", "bstq_solve_noalloc",
-           "bstq_syev_work_size", "bstq_syev", "bstq_stedc_leaves_work_size", "bstq_stedc_leaves")
+           "bstq_syev_work_size", "bstq_syev", "bstq_stedc_leaves_work_size", "bstq_stedc_leaves",
+           "bstq_diag_work_size", "bstq_diag")
+
+# Diagnostic ops (bstq_diag): one building block of the solve on a table of
+# inputs; values in and out per record.
+DIAG_RCP, DIAG_DIV, DIAG_SQRT, DIAG_RSQRT, DIAG_HYP1 = 1, 2, 3, 4, 5
+DIAG_LARTG, DIAG_LARTG_FAST, DIAG_SHIFT = 6, 7, 8
+DIAG_PASS_STATIC, DIAG_PASS_DYN_EXP, DIAG_PASS_DYN_PG = 20, 21, 22
+DIAG_FASTQ = 30
+DIAG_SHAPE = {DIAG_RCP: (1, 1), DIAG_DIV: (2, 1), DIAG_SQRT: (1, 1), DIAG_RSQRT: (1, 1), DIAG_HYP1: (1, 1),
+              DIAG_LARTG: (2, 3), DIAG_LARTG_FAST: (2, 3), DIAG_SHIFT: (3, 4),
+              DIAG_PASS_STATIC: (42, 288), DIAG_PASS_DYN_EXP: (42, 288), DIAG_PASS_DYN_PG: (42, 288)}
 
 
 class Params(ctypes.Structure):
@@ -95,6 +106,10 @@ def load(path: str = LIB_PATH):
         lib.bstq_stedc_leaves.restype = ctypes.c_int
         lib.bstq_stedc_leaves.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp,
                                           vp, vp, vp, P]
+        lib.bstq_diag_work_size.restype = sz
+        lib.bstq_diag_work_size.argtypes = [ctypes.c_int, ctypes.c_int, i64]
+        lib.bstq_diag.restype = ctypes.c_int
+        lib.bstq_diag.argtypes = [ctypes.c_int, ctypes.c_int, i64, ctypes.c_int, vp, vp, vp, vp]
         lib.bstq_solve_noalloc.restype = ctypes.c_int
         lib.bstq_solve_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp,
                                            vp, P]
@@ -329,3 +344,25 @@ def stedc_leaves(d, e, leaf: int, jobz: bool = True, work=None, stream=None, **p
         if t:
             Qt = Q[batch * F * L * L:].view(batch, t, t).transpose(1, 2)
     return d, Qf, Qt, info
+
+
+def diag(op: int, inp, count: int, arg: int = 0, stream=None):
+    """bstq_diag on a CUDA tensor ``inp`` (float32 or float64, the records of
+    ``count`` inputs back to back).  Returns the (count, values out) result
+    tensor.  Nothing is synchronised."""
+    import torch
+    if not (inp.is_cuda and inp.is_contiguous()):
+        raise ValueError("bstq.diag: inp must be a contiguous CUDA tensor")
+    code = _dtype_code(inp.dtype)
+    out_per = 256 if op == DIAG_FASTQ else DIAG_SHAPE[op][1]
+    out = torch.empty((count, out_per), dtype=inp.dtype, device=inp.device)
+    lib = load()
+    wbytes = int(lib.bstq_diag_work_size(int(op), code, int(count)))
+    if wbytes == 0:
+        raise BstqError(-1, "bstq_diag_work_size")
+    work = torch.empty(wbytes, dtype=torch.uint8, device=inp.device)
+    rc = lib.bstq_diag(int(op), code, int(count), int(arg), inp.data_ptr(), out.data_ptr(), work.data_ptr(),
+                       _stream_handle(stream))
+    if rc != 0:
+        raise BstqError(rc, "bstq_diag")
+    return out

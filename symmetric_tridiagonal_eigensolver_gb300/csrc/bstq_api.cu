@@ -10,6 +10,7 @@
 
 #include "../../include/bstq.h"
 #include "bstq_split.cuh"
+#include "bstq_diag.h"
 #include "bstq_leaves.h"
 #include "bstq_plan.h"
 #include "bstq_registry.h"
@@ -127,8 +128,27 @@ int memory_rows(int dtype, int nm, int qs)
     return qs == QS_REG ? 0 : ((nm - rr + w - 1) / w) * w;
 }
 
-// Default scheduler per (dtype, chunk): flat lockstep.
-int default_sched(int, int) { return SCHED_FLAT; }
+// Default scheduler per (dtype, jobz, compile-time size), chosen from
+// measurement as the BatchLAS page "perf_steqr" (section "Lockstep flat
+// solver") chooses it per (dtype, chunk).  GB300, batch 65,536 for n <= 8
+// and 32,768 above, L2 flushed, medians of five interleaved rounds of 15
+// steps (ms, flat against nested on the default family):
+//   float n <= 4, V and N: nested (n = 3 V 0.0123 / 0.0143, n = 4 V
+//     0.0164 / 0.0172, n = 4 N 0.0151 / 0.0168);
+//   float 5 <= n <= 8, N: nested (n = 6 0.0246 / 0.0266; n = 5 and 8
+//     equal);  V: flat (n = 5 0.0373 / 0.0389, n = 6 0.0529 / 0.0492,
+//     n = 8 equal);
+//   double n <= 4, V: nested, on the static-position family (n = 3 0.1024
+//     against 0.1168 for the dynamic family either way, n = 4 0.1751 against
+//     0.2103);
+//   all other sizes: flat (float n = 12 V 0.053 / 0.062, n = 16 V
+//     0.109 / 0.117, n = 32 V 1.95 / 3.39; double within 0.5 %).
+int default_sched(int dtype, int jobz, int nm)
+{
+    if (dtype == BSTQ_F32)
+        return (nm <= 4 || (nm <= 8 && !jobz)) ? SCHED_NESTED : SCHED_FLAT;
+    return (nm <= 4 && jobz) ? SCHED_NESTED : SCHED_FLAT;
+}
 
 // Default kernel family (static positions in registers, or dynamic
 // positions with d and e in shared memory), per (dtype, jobz, n) from
@@ -140,11 +160,14 @@ int default_sched(int, int) { return SCHED_FLAT; }
 //          FP64-bound, and the dynamic kernel has no union of position
 //          ranges and a factored Q update;
 //   n > 32: dynamic (the static family is built up to n = 32).
-int default_family(int dtype, int jobz, int nm)
+//   double n <= 4, V, under the nested scheduler: static (n = 4 V 0.175
+//          against 0.210 ms; flat: 0.202 against 0.211).
+int default_family(int dtype, int jobz, int nm, int sched)
 {
-    (void)jobz;
     if (nm > 32)
         return FAMILY_DYNAMIC;  // the only family built above n = 32
+    if (dtype == BSTQ_F64 && jobz && nm <= 4 && sched == SCHED_NESTED)
+        return FAMILY_STATIC;
     return dtype == 0 ? FAMILY_STATIC : FAMILY_DYNAMIC;
 }
 
@@ -194,11 +217,12 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
             break;
         }
     const bool pg = p && p->update_scheme == 1;
+    const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, jobz, nm);
     const int family = force_family ? force_family
-                                    : (p && p->kernel) ? p->kernel : (pg ? FAMILY_DYNAMIC : default_family(dtype, jobz, nm));
+                       : (p && p->kernel) ? p->kernel
+                                          : (pg ? FAMILY_DYNAMIC : default_family(dtype, jobz, nm, sched));
     if (pg && family == FAMILY_STATIC)
         return -10;  // the PG step runs in the dynamic-position kernels only
-    const int sched = (p && p->scheduler) ? p->scheduler : default_sched(dtype, nm);
     int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm, sched)) : 0;
     if (family != FAMILY_STATIC && jobz)
         qs = QS_GLOBAL;  // the dynamic kernels keep Q in global scratch
@@ -215,11 +239,9 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         // (four warpgroups), up to 32 * kSplitLivePairs problems per block,
         // spread evenly over the SMs; shared memory as SplitSmem<nm>
         const int P = kSplitLivePairs;
-        const int rr = nm <= 8 ? nm : 8;
-        size_t off = 2ull * nm * 4 * 32 * P + size_t(P) * 2 * nm * 32 * 8 + size_t(P) * 2 * 8 +
-                     size_t(P) * 32 * (16 + nm);
-        off = (off + 15) / 16 * 16;
-        pl.smem = off + size_t(P) * 32 * nm * (nm - rr) * 4;
+        if (nm != 12 && nm != 16)
+            return -10;
+        pl.smem = nm == 12 ? SplitSmem<12>::total : SplitSmem<16>::total;
         pl.tpb = 64 * kSplitPairs;
         if (p && p->threads_per_block && p->threads_per_block != pl.tpb)
             return -10;
@@ -728,6 +750,41 @@ extern "C" const char *bstq_status_string(int code)
 extern "C" const char *bstq_version(void) { return "bstq 0.1.0 sm_103a"; }
 
 extern "C" const char *bstq_last_error(void) { return g_last_error; }
+
+extern "C" size_t bstq_diag_work_size(int op, bstq_dtype dtype, int64_t count)
+{
+    if ((dtype != BSTQ_F32 && dtype != BSTQ_F64) || count < 0 || diag_check_op(op, dtype == BSTQ_F64) != 0)
+        return 0;
+    return diag_work_bytes(op, dtype == BSTQ_F64, count);
+}
+
+extern "C" int bstq_diag(int op, bstq_dtype dtype, int64_t count, int arg, const void *in, void *out, void *work,
+                         void *stream)
+{
+    if (dtype != BSTQ_F32 && dtype != BSTQ_F64)
+        return -2;
+    const int f64 = dtype == BSTQ_F64;
+    if (diag_check_op(op, f64) != 0)
+        return -1;
+    if (count < 0 || count > (1LL << 36))
+        return -3;
+    if (op == BSTQ_DIAG_FASTQ && (arg < 0 || arg > 1000000))
+        return -4;
+    if (count == 0)
+        return 0;
+    const size_t elem = f64 ? 8 : 4;
+    if (misaligned(in, elem) || !in)
+        return -5;
+    if (misaligned(out, elem) || !out)
+        return -6;
+    if (diag_uses_work(op) && (!work || misaligned(work, 16)))
+        return -7;
+    DevInfo di;
+    if (!dev_info(di))
+        return BSTQ_ERR_NODEVICE;
+    const cudaError_t err = launch_diag(op, f64, count, arg, in, out, work, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? 0 : cuda_fail(err, "diagnostic launch");
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.

@@ -483,6 +483,46 @@ struct DynLane {
             step_q_carry(cs, sn);
     }
 
+    // Fast-Givens scales drift: every rotation multiplies the two deltas it
+    // touches by max(|cs|, |sn|) >= 1/sqrt(2) and nothing restores them, so
+    // a column rotated a couple of thousand times (a large sweep budget at
+    // large n) would see delta underflow and 1/delta overflow.  Before each
+    // rotation a delta below 2^-128 is folded into its column of Qt
+    // (Q = Qt diag(delta) is unchanged) and reset to one, which keeps every
+    // delta above 2^-129 and every entry of Qt below 2^129.  The exponent
+    // tests run on the integer pipe; the folds themselves are rare.
+    __device__ __forceinline__ static bool scale_low(T x)
+    {
+        return ((unsigned)(__double2hiint(x) >> 20) & 0x7ffu) < 1023u - 128u;
+    }
+    // the carried column (registers)
+    __device__ __forceinline__ void renorm_carried()
+    {
+        if (scale_low(da)) {
+#pragma unroll
+            for (int j = 0; j < NE; ++j)
+                cur[j] *= da;
+            da = T(1);
+            ia = T(1);
+        }
+    }
+    // column k in the scratch, with its scale dk and inverse ik
+    __device__ __forceinline__ void renorm_mem(int k, T &dk, T &ik)
+    {
+        if (scale_low(dk)) {
+            for (int g = 0; g < Q_::G; ++g) {
+                typename Q_::V16 v = q.vec(k, g);
+                v.a *= dk;
+                v.b *= dk;
+                q.vec(k, g) = v;
+            }
+            dk = T(1);
+            ik = T(1);
+            sdl[k * ms] = T(1);
+            sil[k * ms] = T(1);
+        }
+    }
+
     // step_q_carry for double above n = 32: column C-1 is read four 16-byte
     // vectors at a time, the next group's reads issued before this group's
     // writes, so only the carried column and two groups are live in
@@ -497,7 +537,9 @@ struct DynLane {
         bool f1 = true;
         typename El<T>::R rr;
         if constexpr (FASTQ) {
-            const T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
+            T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
+            renorm_carried();
+            renorm_mem(C - 1, db, ib);
             f1 = (__double_as_longlong(cs) & 0x7fffffffffffffffll) >=
                  (__double_as_longlong(sn) & 0x7fffffffffffffffll);
             const T rp = rcp_nr(f1 ? cs : sn);
@@ -574,9 +616,11 @@ struct DynLane {
             //   x' = y + M x, y' = x - P y, da' = sn db, db' = -sn da;
             // with t = sn/cs (form 1) or cs/sn (form 2), P = t db/da,
             // M = t da/db.  Either way Qt' diag(delta') = Qt diag(delta) G.
+            T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
+            renorm_carried();
+            renorm_mem(C - 1, db, ib);
             E nx[NE];
             q.load(C - 1, nx);
-            const T db = sdl[(C - 1) * ms], ib = sil[(C - 1) * ms];
             const bool f1 = (__double_as_longlong(cs) & 0x7fffffffffffffffll) >=
                             (__double_as_longlong(sn) & 0x7fffffffffffffffll);
             const T rp = rcp_nr(f1 ? cs : sn);

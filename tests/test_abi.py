@@ -65,6 +65,20 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
     assert lib.bstq_work_size(0, 1, 40, 10) == 0
     assert lib.bstq_solve_host(0, 1, 8, 10, None, good, good, good, good, None, None) == -5
+    # the diagnostic entry point
+    diag = lib.bstq_diag
+    assert diag(99, 0, 10, 0, good, good, good, None) == -1          # unknown op
+    assert diag(bstq.DIAG_FASTQ, 0, 10, 5, good, good, good, None) == -1   # double only
+    assert diag(bstq.DIAG_RCP, 7, 10, 0, good, good, good, None) == -2
+    assert diag(bstq.DIAG_RCP, 0, -1, 0, good, good, good, None) == -3
+    assert diag(bstq.DIAG_FASTQ, 1, 10, -1, good, good, good, None) == -4
+    assert diag(bstq.DIAG_RCP, 0, 0, 0, None, None, None, None) == 0     # empty: no-op
+    assert diag(bstq.DIAG_RCP, 0, 10, 0, None, good, None, None) == -5
+    assert diag(bstq.DIAG_RCP, 1, 10, 0, mis, good, None, None) == -5
+    assert diag(bstq.DIAG_RCP, 0, 10, 0, good, None, None, None) == -6
+    assert diag(bstq.DIAG_PASS_DYN_EXP, 0, 10, 0, good, good, None, None) == -7
+    assert lib.bstq_diag_work_size(bstq.DIAG_PASS_DYN_PG, 1, 100) >= 100 * 16 * 16 * 8
+    assert lib.bstq_diag_work_size(99, 1, 100) == 0
 
 
 def test_no_device_is_reported_not_faked(lib):
