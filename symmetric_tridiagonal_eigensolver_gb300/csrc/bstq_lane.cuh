@@ -305,6 +305,27 @@ struct QMix {
                 cur[j] = nx[j];
         }
     }
+    // Column s (static s in an unrolled loop) straight to global memory at
+    // qc: the register rows and the memory rows go out as separate 16-byte
+    // vectors, so no whole-column temporary is live beside the register
+    // rows.  Needs 16-byte aligned columns of exactly RR + MR rows.
+    __device__ __forceinline__ void store_col_direct(int s, T *qc) const
+    {
+        static_assert(NER % 2 == 0, "register rows in whole 16-byte vectors");
+        V16 *dst = reinterpret_cast<V16 *>(qc);
+#pragma unroll
+        for (int k = 0; k < NM; ++k)
+            if (k == s) {
+#pragma unroll
+                for (int v = 0; v < NER / 2; ++v)
+                    dst[v] = V16{qr[k][2 * v], qr[k][2 * v + 1]};
+            }
+        if constexpr (NEM > 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                dst[NER / 2 + g] = base[vidx(s, g)];
+        }
+    }
     // Column s (static s in an unrolled loop), all stored rows, into out[].
     __device__ __forceinline__ void get_col(int s, T (&out)[RR + MR])
     {

@@ -137,6 +137,7 @@ struct SplitSmem {
     static constexpr size_t off_qmem = (off_hand + hand + 15) / 16 * 16;
     static constexpr size_t total = off_qmem + qmem;
 };
+static_assert(SplitSmem<16>::total <= 232448, "split-role shared memory exceeds the per-block maximum");
 
 template <int NM, int SCHED>
 __global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams p)
@@ -285,12 +286,20 @@ __global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams 
                     qout[i] = __int_as_float(0x7fffffff);
             } else {
                 const bool vec = q_vector_ok<float>(p.Q, n);
+                if (vec && n == NM) {
+                    // whole aligned columns: register and shared rows written
+                    // as they are held
 #pragma unroll
-                for (int s = 0; s < NM; ++s) {
-                    if (s < n) {
-                        float col[NM];
-                        A.Q.get_col(s, col);
-                        store_col(qout + (long long)hpos[s * 32 * P] * n, col, n, vec);
+                    for (int s = 0; s < NM; ++s)
+                        A.Q.store_col_direct(s, qout + (long long)hpos[s * 32 * P] * n);
+                } else {
+#pragma unroll
+                    for (int s = 0; s < NM; ++s) {
+                        if (s < n) {
+                            float col[NM];
+                            A.Q.get_col(s, col);
+                            store_col(qout + (long long)hpos[s * 32 * P] * n, col, n, vec);
+                        }
                     }
                 }
             }
