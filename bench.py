@@ -41,6 +41,11 @@ COMPANIONS = [dict(dtype="float32", n=8, batch=65536, jobz=True),
               dict(dtype="float32", n=16, batch=32768, jobz=False),
               dict(dtype="float64", n=12, batch=32768, jobz=True),
               dict(dtype="float64", n=12, batch=32768, jobz=False)]
+# The small case (float32 n = 4, batch 1,024, V) and the mixed hard-case
+# batch at n = 32 in both precisions and both jobz.
+SMALL_CASE = dict(dtype="float32", n=4, batch=1024, jobz=True)
+MIXED = [dict(dtype=dt, n=32, batch=32768, jobz=jz, kind="mixed")
+         for dt in ("float32", "float64") for jz in (True, False)]
 # Context only: steqr_cta float n=16 V, batch 32,768, flat solver, RTX 4090
 # (BatchLAS perf_steqr, "What ships" table: 450.9 us per call).
 PAGES_BASELINE = 32768 / 450.9e-6
@@ -112,7 +117,8 @@ def rank_seed(rank):
 
 
 def wl_name(w):
-    return f"{w['dtype']} n={w['n']} jobz={'V' if w['jobz'] else 'N'} batch={w['batch']} N(0,1) seed 0"
+    kind = "mixed hard cases" if w.get("kind", "normal") == "mixed" else "N(0,1)"
+    return f"{w['dtype']} n={w['n']} jobz={'V' if w['jobz'] else 'N'} batch={w['batch']} {kind} seed 0"
 
 
 def algorithmic(w, counts):
@@ -209,7 +215,7 @@ def time_workload(w, steps, warmup, dist_barrier, flush, stream, seed=0, min_war
     import torch
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
     dt = np.float32 if w["dtype"] == "float32" else np.float64
-    d, e = inputs.normal_problems(w["n"], w["batch"], dt, seed=seed)
+    d, e = inputs.problems(w.get("kind", "normal"), w["n"], w["batch"], dt, seed=seed)
     dev = torch.device("cuda")
     d0 = torch.from_numpy(d).to(dev)
     eg = torch.from_numpy(e).to(dev)
@@ -348,8 +354,37 @@ def cpu_baseline(w, seconds=12.0):
         oracle.steqr(d[:sample2], e[:sample2], jobz=w["jobz"], nthreads=cores)
     t1 = time.perf_counter()
     rate = sample2 * reps / (t1 - t0)
+    # one thread, on a sample sized for about a quarter of `seconds`
+    one = int(min(w["batch"], max(256, rate / cores * seconds / 4)))
+    t0 = time.perf_counter()
+    oracle.steqr(d[:one], e[:one], jobz=w["jobz"], nthreads=1)
+    t1 = time.perf_counter()
     return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"first {sample2} problems of the batch x {reps}, {cores} threads"}
+            "sample": f"first {sample2} problems of the batch x {reps}, {cores} threads",
+            "one_thread": {"value": one / (t1 - t0), "unit": UNIT, "cores": 1,
+                           "sample": f"first {one} problems of the batch, 1 thread"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    platform string)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args, rank, world):
@@ -383,6 +418,22 @@ def run_reference(args, rank, world):
     return 0
 
 
+def run_alu_peaks():
+    """Compile alu_peaks.cu for sm_103a in a temporary directory, run it on
+    the current GPU and print its JSON line (context for the derived
+    FP32 / FP64 peaks of the roofline)."""
+    import shutil
+    import tempfile
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "alu_peaks")
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe,
+                        os.path.join(ROOT, "alu_peaks.cu")], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.strip()
+    print(out)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,6 +441,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-companions", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the n = 1..32 sweep of the companions")
+    ap.add_argument("--alu-peaks", action="store_true",
+                    help="build and run alu_peaks.cu (FP32 / FP64 FMA throughput) and print its line")
     ap.add_argument("--sched", type=int, default=0, help="0 auto, 1 flat, 2 nested (with --only)")
     ap.add_argument("--qstore", type=int, default=0, help="Q storage policy (with --only)")
     ap.add_argument("--kernel", type=int, default=0, help="kernel family 1 static, 2 dynamic (with --only)")
@@ -406,6 +460,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.alu_peaks:
+        return run_alu_peaks()
 
     import torch
     import torch.distributed as tdist
@@ -459,17 +515,45 @@ def main():
     e2e_ms, h2d, d2h = time_e2e(HEADLINE, max(3, args.steps // 4), 2, stream)
 
     workloads = {}
+    counts_cache = {}
+
+    def measure(w, steps, **params):
+        """Time workload w (with solver parameters) and price it against the
+        roofline from the oracle's counts on the same input."""
+        wm, wd, we, wdesc = time_workload(w, steps, 3, lambda: None, flush, stream, **params)
+        key = wl_name(w)
+        if key not in counts_cache:
+            counts_cache[key] = oracle_counts(w, wd, we)
+        fl, by = algorithmic(w, counts_cache[key])
+        peak = fp32_peak if w["dtype"] == "float32" else fp64_peak
+        t = statistics.mean(wm) / 1e3
+        roof_t = max(fl / peak, by / hbm_peak)
+        return {"problems_per_s": w["batch"] / t, "ms": t * 1e3, "roofline_fraction": roof_t / t,
+                "kernel": wdesc, "gflop": fl / 1e9, "mb": by / 1e6}
+
     if rank == 0 and not args.no_companions:
+        csteps = max(5, args.steps // 2)
+        for w in [SMALL_CASE] + COMPANIONS + MIXED:
+            workloads[wl_name(w)] = measure(w, csteps)
+        # flat lockstep against the nested loop, each forced, for the float
+        # n = 8 / 16 and double n = 12 workloads
         for w in COMPANIONS:
-            wm, wd, we, wdesc = time_workload(w, max(5, args.steps // 2), 3, lambda: None, flush, stream)
-            c = oracle_counts(w, wd, we)
-            fl, by = algorithmic(w, c)
-            peak = fp32_peak if w["dtype"] == "float32" else fp64_peak
-            t = statistics.mean(wm) / 1e3
-            roof_t = max(fl / peak, by / hbm_peak)
-            workloads[wl_name(w)] = {"problems_per_s": w["batch"] / t, "ms": t * 1e3,
-                                     "roofline_fraction": roof_t / t, "kernel": wdesc,
-                                     "gflop": fl / 1e9, "mb": by / 1e6}
+            for sched, nm in ((1, "flat"), (2, "nested")):
+                workloads[f"scheduler {nm}: {wl_name(w)}"] = measure(w, csteps, scheduler=sched)
+        # n = 1 .. 32 in both precisions and both jobz (batch 65,536 for
+        # n <= 8, else 32,768)
+        if not args.no_sweep:
+            sweep = {}
+            for dtype in ("float32", "float64"):
+                for jobz in (True, False):
+                    rows = []
+                    for n in range(1, 33):
+                        w = dict(dtype=dtype, n=n, batch=65536 if n <= 8 else 32768, jobz=jobz)
+                        r = measure(w, 3)
+                        rows.append([n, round(r["problems_per_s"]), round(r["roofline_fraction"], 4),
+                                     round(r["ms"], 4)])
+                    sweep[f"{dtype} jobz={'V' if jobz else 'N'}"] = rows
+            workloads["sweep n=1..32 (n, problems/s, roofline fraction, ms)"] = sweep
         for dtype, n in (("float32", 16), ("float64", 12)):
             ms_s = time_syev(n, 32768, dtype, True, max(5, args.steps // 2), 3, flush, stream)
             workloads[f"fused syev {dtype} n={n} jobz=V batch=32768 dense N(0,1) seed 0"] = {
