@@ -115,7 +115,7 @@ typedef enum {
 
 #define BSTQ_ERR_CUDA 1
 #define BSTQ_ERR_NODEVICE 2
-#define BSTQ_MAX_N 64
+#define BSTQ_MAX_N 128
 
 /* Bytes of device workspace bstq_solve needs for (dtype, jobz, n, batch)
  * with default parameters: int32 info[batch] at offset 0, then any scratch
@@ -128,7 +128,7 @@ size_t bstq_work_size_ex(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
                          const bstq_params *p);
 
 /*
- * Solve `batch` problems of size n (1 <= n <= 64; above 32 the dynamic-position
+ * Solve `batch` problems of size n (1 <= n <= 128; above 32 the dynamic-position
  * kernels run, the static family being built up to 32) on `stream`
  * (a cudaStream_t; NULL = legacy default stream).
  *   d     in/out  batch*n values of dtype; on exit the eigenvalues.
@@ -188,7 +188,7 @@ int bstq_solve_host(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch,
  *             p->kernel = BSTQ_KERNEL_STATIC for those sizes returns -10.
  * Returns 0; -2 when jobz is not BSTQ_JOBZ_V; -4 when the problems need more
  * scratch than the array holds (n_pad^2 * sizeof(element) bytes per problem
- * slot, n_pad = n rounded up to 4, 8, 12, 16, 24, 32, 48 or 64, slots = batch rounded up to
+ * slot, n_pad = n rounded up to 4, 8, 12, 16, 24, 32, 48, 64, 96 or 128, slots = batch rounded up to
  * the block size; e.g. about 58,000 double problems of n <= 12 fit, or 16,000
  * float problems of n <= 32); other codes as bstq_solve_ex.
  * The first call on each device looks up the array's device address (with
@@ -244,7 +244,7 @@ int bstq_syev(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t batch, const void
  * diagonal entries next to the boundary (the upper boundary of a leaf
  * first).  Every leaf is then solved as a steqr problem of its own (from
  * the identity, ascending), all leaves of the batch in one batched solve
- * (two when a shorter last leaf exists).  n >= 1, 1 <= leaf <= 64.
+ * (two when a shorter last leaf exists).  n >= 1, 1 <= leaf <= 128.
  *   d     in/out  batch*n values; on exit each leaf's eigenvalues, ascending
  *                 within the leaf, at the leaf's rows.
  *   e     in      batch*(n-1) values (may be NULL when n == 1).

@@ -21,6 +21,9 @@
 #include <pthread.h>
 #include <stddef.h>
 
+/* Largest problem size (the buffers of one problem live on the stack). */
+#define ORACLE_MAX_N 128
+
 #define R_PRESCALE_F32 16777216.0f             /* 2^24 */
 #define R_PRESCALE_F64 9007199254740992.0      /* 2^53 */
 

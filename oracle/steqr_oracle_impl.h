@@ -338,8 +338,8 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort, int scheme,
     /* algo_steqr, final paragraph: ascending order, same permutation on the
      * columns of Q.  Stable: equal values keep their original order. */
     if (sort && n > 1) {
-        int perm[64];
-        real_t val[64];
+        int perm[ORACLE_MAX_N];
+        real_t val[ORACLE_MAX_N];
         for (i = 0; i < n; ++i) {
             perm[i] = i;
             val[i] = d[i];
@@ -359,7 +359,7 @@ static int FN(steqr_one)(int n, int jobz, int maxit_per_n, int sort, int scheme,
         for (i = 0; i < n; ++i)
             d[i] = val[i];
         if (jobz) {
-            real_t tmp[64 * 64];
+            real_t tmp[ORACLE_MAX_N * ORACLE_MAX_N];
             for (i = 0; i < n * n; ++i)
                 tmp[i] = Q[i];
             for (int j = 0; j < n; ++j)
@@ -508,7 +508,7 @@ static void *FN(worker)(void *arg)
 {
     FN(job_t) *jb = (FN(job_t) *)arg;
     const int n = jb->n;
-    real_t ework[64];
+    real_t ework[ORACLE_MAX_N];
     for (long b = jb->b0; b < jb->b1; ++b) {
         real_t *db = jb->d + b * n;
         const real_t *eb = jb->e + b * (n > 1 ? n - 1 : 0);
@@ -596,7 +596,7 @@ int FN(oracle_steqr_batch)(int n, long batch, int jobz, int maxit_per_n,
                            int sort, real_t *d, const real_t *e, real_t *Q,
                            int *info, long *counters, int nthreads, int scheme)
 {
-    if (n < 1 || n > 64 || batch < 0 || maxit_per_n < 0 || scheme < 0 || scheme > 1)
+    if (n < 1 || n > ORACLE_MAX_N || batch < 0 || maxit_per_n < 0 || scheme < 0 || scheme > 1)
         return -1;
     if (nthreads < 1)
         nthreads = 1;

@@ -22,7 +22,7 @@ QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID, QSTO
 KERNEL_AUTO, KERNEL_STATIC, KERNEL_DYNAMIC = 0, 1, 2
 UPDATE_EXP, UPDATE_PG = 0, 1
 ERR_CUDA, ERR_NODEVICE = 1, 2
-MAX_N = 64
+MAX_N = 128
 
 # Every symbol include/bstq.h declares.
 EXPORTS = ("bstq_work_size", "bstq_work_size_ex", "bstq_solve", "bstq_solve_ex",

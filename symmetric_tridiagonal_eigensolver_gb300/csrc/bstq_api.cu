@@ -9,7 +9,7 @@
 #include <mutex>
 
 #include "../../include/bstq.h"
-#include "bstq_split.cuh"
+#include "bstq_split2.cuh"
 #include "bstq_diag.h"
 #include "bstq_leaves.h"
 #include "bstq_plan.h"
@@ -28,7 +28,7 @@ struct Plan {
     int ppb = 0;  // problems per block (split-role kernel)
 };
 
-constexpr int kNmList[] = {4, 8, 12, 16, 24, 32, 48, 64};
+constexpr int kNmList[] = {4, 8, 12, 16, 24, 32, 48, 64, 96, 128};
 constexpr int kSyevMaxN = 32;  // the fused syev kernels are built up to n = 32
 
 thread_local char g_last_error[256] = "";
@@ -102,6 +102,10 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched, in
 //   float 9 <= n <= 16, flat scheduler: split roles (chase warps record the
 //     rotations, Q warps apply them; n=16 V 0.131 vs 0.138 ms hybrid, n=12 V
 //     0.072 vs 0.077 ms registers);
+//   float 17 <= n <= 32, flat scheduler: split roles with each problem's Q
+//     rows spread over several Q warps (bstq_split2.cuh; n = 17 V 0.219 vs
+//     0.362 ms hybrid, n = 24 V 0.287 vs 0.487, n = 27 V 0.775 vs 1.70,
+//     n = 32 V 0.813 vs 1.98);
 //   float n <= 12 otherwise: registers; float n >= 16 otherwise: 8 rows of Q
 //     in registers, the rest streamed from shared memory (one wave of 32768
 //     problems stays resident);
@@ -112,7 +116,7 @@ int default_qstore(int dtype, int nm, int sched)
     if (dtype == 0) {
         if (nm <= 8)
             return QS_REG;
-        if (nm <= 16 && sched == SCHED_FLAT)
+        if (nm <= 32 && sched == SCHED_FLAT)
             return QS_SPLIT;
         return nm <= 12 ? QS_REG : QS_HYBRID;
     }
@@ -234,6 +238,30 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         cudaGetLastError();
         return BSTQ_ERR_NODEVICE;
     }
+    if (qs == QS_SPLIT && (nm == 24 || nm == 32)) {
+        // several Q warps per chase warp (bstq_split2.cuh): fixed block
+        // shape, 32 problems per group of warps, as many blocks as the
+        // batch needs (one block per SM at a time)
+        const int threads = nm == 24 ? Split2ShapeOf<24>::THREADS : Split2ShapeOf<32>::THREADS;
+        const int per_block = 32 * (nm == 24 ? Split2Cfg<24>::G : Split2Cfg<32>::G);
+        pl.smem = nm == 24 ? Split2ShapeOf<24>::total : Split2ShapeOf<32>::total;
+        pl.tpb = threads;
+        if (p && p->threads_per_block && p->threads_per_block != pl.tpb)
+            return -10;
+        if (fa.maxThreadsPerBlock < pl.tpb || pl.smem > (size_t)di.max_smem_block)
+            return -10;
+        // spread the problems evenly over the SMs when one wave holds them
+        long long ppb = batch > 0 ? (batch + di.sms - 1) / di.sms : 1;
+        if (ppb > per_block)
+            ppb = per_block;
+        pl.ppb = (int)ppb;
+        pl.grid = batch > 0 ? (batch + ppb - 1) / ppb : 0;
+        pl.qwork_bytes = 0;
+        pl.work_bytes = align256(size_t(batch) * 4);
+        if (pl.work_bytes == 0)
+            pl.work_bytes = 256;
+        return 0;
+    }
     if (qs == QS_SPLIT) {
         // fixed shape: kSplitPairs chase warps + kSplitPairs Q warps per block
         // (four warpgroups), up to 32 * kSplitLivePairs problems per block,
@@ -275,6 +303,9 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         // d and e in shared memory, plus the column scales of the factored
         // double eigenvector update
         smem_per_thread = 2 * size_t(nm) * elem + ((dtype == BSTQ_F64 && jobz) ? 2 * size_t(nm) * elem : 0);
+        // the carried eigenvector column above n = 64
+        if (jobz && nm > 64)
+            smem_per_thread += size_t(nm) * elem;
     }
     // Threads an SM can hold for this kernel.
     const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
@@ -734,7 +765,7 @@ extern "C" const char *bstq_status_string(int code)
     case BSTQ_ERR_NODEVICE: return "no usable CUDA device is current";
     case -1: return "invalid dtype";
     case -2: return "invalid jobz";
-    case -3: return "n outside [1, 64]";
+    case -3: return "n outside [1, 128]";
     case -4: return "invalid batch (bstq_solve_noalloc: more problems than its fixed scratch array holds)";
     case -5: return "d is NULL or misaligned";
     case -6: return "e is NULL or misaligned";

@@ -91,6 +91,59 @@ struct DynQ {
     }
 };
 
+// One bit per entry for problems of 65 to 128 entries: two 64-bit words,
+// kept as two scalars (an array member, even indexed with constants, sent
+// the whole lane structure to local memory), with the few operations the
+// lane's block bookkeeping needs; the 32- and 64-bit masks use the plain
+// integer operators.
+struct Mask128 {
+    unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void mask_clear(unsigned &m) { m = 0u; }
+__device__ __forceinline__ void mask_clear(unsigned long long &m) { m = 0ull; }
+__device__ __forceinline__ void mask_clear(Mask128 &m) { m.lo = m.hi = 0ull; }
+__device__ __forceinline__ void mask_set(unsigned &m, int i) { m |= 1u << i; }
+__device__ __forceinline__ void mask_set(unsigned long long &m, int i) { m |= 1ull << i; }
+__device__ __forceinline__ void mask_set(Mask128 &m, int i)
+{
+    const unsigned long long bit = 1ull << (i & 63);
+    m.lo |= i < 64 ? bit : 0ull;
+    m.hi |= i < 64 ? 0ull : bit;
+}
+__device__ __forceinline__ bool mask_test(unsigned m, int i) { return (m >> i) & 1u; }
+__device__ __forceinline__ bool mask_test(unsigned long long m, int i) { return (m >> i) & 1ull; }
+__device__ __forceinline__ bool mask_test(const Mask128 &m, int i)
+{
+    return ((i < 64 ? m.lo : m.hi) >> (i & 63)) & 1ull;
+}
+// every bit from i on (i >= 0)
+__device__ __forceinline__ void mask_set_from(unsigned &m, int i) { m |= i < 32 ? (~0u << i) : 0u; }
+__device__ __forceinline__ void mask_set_from(unsigned long long &m, int i) { m |= i < 64 ? (~0ull << i) : 0ull; }
+__device__ __forceinline__ void mask_set_from(Mask128 &m, int i)
+{
+    m.lo |= i < 64 ? (~0ull << i) : 0ull;
+    m.hi |= i <= 64 ? ~0ull : (i < 128 ? (~0ull << (i - 64)) : 0ull);
+}
+__device__ __forceinline__ bool mask_any(unsigned m) { return m != 0u; }
+__device__ __forceinline__ bool mask_any(unsigned long long m) { return m != 0ull; }
+__device__ __forceinline__ bool mask_any(const Mask128 &m) { return (m.lo | m.hi) != 0ull; }
+// Block [lb, le] containing index s from a boundary mask (bit i set when
+// e_i is an exact zero or i >= n-1): the first set bit at or after s, and
+// one past the last set bit before s.
+__device__ __forceinline__ int block_hi(const Mask128 &m, int s)
+{
+    const unsigned long long xl = s < 64 ? (m.lo >> s) << s : 0ull;
+    const unsigned long long xh = s <= 64 ? m.hi : (m.hi >> (s - 64)) << (s - 64);
+    return xl ? __ffsll((long long)xl) - 1 : (xh ? 64 + __ffsll((long long)xh) - 1 : 127);
+}
+__device__ __forceinline__ int block_lo(const Mask128 &m, int s)
+{
+    const unsigned long long xl = s >= 64 ? m.lo : (s > 0 ? m.lo & ((1ull << s) - 1ull) : 0ull);
+    const unsigned long long xh = s >= 128 ? m.hi : (s > 64 ? m.hi & ((1ull << (s - 64)) - 1ull) : 0ull);
+    return xh ? 128 - __clzll((long long)xh) : (xl ? 64 - __clzll((long long)xl) : 0);
+}
+
 // double eigenvectors are accumulated in factored form Q = Qt diag(delta)
 // (fast Givens, after Gentleman): a rotation then costs two FMAs per row
 // instead of two multiplies and two FMAs, plus a dozen scalar operations for
@@ -109,14 +162,21 @@ struct DynLane {
     static constexpr int NE = Q_::NE;
     static constexpr bool FASTQ = dyn_fastq<T, WANTZ>();
     // Block-boundary and mirror masks: one bit per entry.
-    using Mask = typename std::conditional<(NM > 32), unsigned long long, unsigned>::type;
-    static constexpr int MASK_BITS = 8 * (int)sizeof(Mask);
+    static_assert(NM <= 128, "block masks hold up to 128 entries");
+    using Mask = typename std::conditional<
+        (NM > 64), Mask128, typename std::conditional<(NM > 32), unsigned long long, unsigned>::type>::type;
     // The column shared by successive rotations of a sweep stays in
-    // registers.  For double above n = 32 the whole next column would not
-    // fit beside it, so that column is read and rotated in groups of vectors
-    // (step_q_carry_chunked); float reads the whole next column at once
-    // (up to 32 packed pairs), which measured faster.
-    static constexpr bool CHUNKED = sizeof(T) == 8 && NM > 32;
+    // registers.  For double above n = 32, and float above n = 64, the whole
+    // next column would not fit beside it, so that column is read and
+    // rotated in groups of vectors and the carried one is kept in shared
+    // memory (step_q_carry_chunked); float up to n = 64 reads the whole
+    // next column at once (up to 32 packed pairs), which measured faster.
+    static constexpr bool CHUNKED = (sizeof(T) == 8 && NM > 32) || NM > 64;
+    // Above n = 64 the carried column itself lives in shared memory; at
+    // n = 48 and 64 (double) it stays in registers, which measured faster
+    // (f64 n = 64 V 169 against 221 ms, n = 48 45 against 77 ms): the extra
+    // shared memory per thread cost a warp of occupancy.
+    static constexpr bool CARRY_SMEM = NM > 64;
 
     T *sd, *se;  // this lane's d and e in shared memory
     T *sdl, *sil;  // column scales delta_j and 1/delta_j (FASTQ)
@@ -138,7 +198,16 @@ struct DynLane {
     int L, C;      // steps of the current task, current position
     T a_reg, b_reg;  // d_C and e_{C-1} as updated by the previous step
     Q_ q;
-    E cur[NE];     // Q column C (the column shared with the next rotation)
+    E cur[CARRY_SMEM ? 1 : NE];  // Q column C (the column shared with the next rotation)
+    E *scr;        // CARRY_SMEM: that column in shared memory instead,
+                   // element j at scr[j * ms]
+    __device__ __forceinline__ E &carry(int j)
+    {
+        if constexpr (CARRY_SMEM)
+            return scr[j * ms];
+        else
+            return cur[j];
+    }
 
     __device__ __forceinline__ T D(int i) const { return sd[i * ms]; }
     __device__ __forceinline__ T Ev(int i) const { return se[i * ms]; }
@@ -148,7 +217,7 @@ struct DynLane {
     __device__ __forceinline__ int phys(int s) const
     {
         int a = block_lo(zmask, s), b = block_hi(zmask, s);
-        return ((revmask >> a) & 1) ? (a + b - s) : s;
+        return mask_test(revmask, a) ? (a + b - s) : s;
     }
 
     __device__ __forceinline__ void scale_factors(T an, int &isc, T &pr, T &s, T &ae) const
@@ -190,7 +259,7 @@ struct DynLane {
         bnext = 0;
         lb = le = lo = m = 0;
         info = 0;
-        revmask = 0;
+        mask_clear(revmask);
         iscale = 0;
         pre = sc = aeff = anorm = T(1);
         f = g = cs2 = sn2 = a_reg = b_reg = T(0);
@@ -198,13 +267,14 @@ struct DynLane {
         C = 0;
         if (!live) {
             status = ST_DEAD;
-            zmask = ~Mask(0);
+            mask_clear(zmask);
+            mask_set_from(zmask, 0);
             return;
         }
         const T *dg = reinterpret_cast<const T *>(p.d) + b * n;
         const T *eg = reinterpret_cast<const T *>(p.e) + b * (n - 1);
         bool bad = false;
-        zmask = 0;
+        mask_clear(zmask);
         for (int i = 0; i < n; ++i) {
             const T di = dg[i];
             const T ei = i < n - 1 ? eg[i] : T(0);
@@ -212,9 +282,9 @@ struct DynLane {
             setE(i, ei);
             bad |= !isfinite(di) || !isfinite(ei);
             if (i >= n - 1 || ei == T(0))
-                zmask |= Mask(1) << i;
+                mask_set(zmask, i);
         }
-        zmask |= n < MASK_BITS ? (~Mask(0) << n) : Mask(0);
+        mask_set_from(zmask, n);
         status = bad ? ST_BAD : ST_RUN;
         if (bad)
             return;
@@ -232,16 +302,16 @@ struct DynLane {
                         y = (y * pr) * s;
                     }
                     if (dabs(x) > dabs(y))
-                        revmask |= Mask(1) << a;
+                        mask_set(revmask, a);
                 }
             }
             a = z + 1;
         }
-        if (revmask) {
+        if (mask_any(revmask)) {
             for (int s = 0; s < n; ++s) {
                 const int ps = phys(s);
                 setD(s, dg[ps]);
-                if (s < n - 1 && !((zmask >> s) & 1)) {
+                if (s < n - 1 && !mask_test(zmask, s)) {
                     const int pn = phys(s + 1);
                     setE(s, eg[ps < pn ? ps : pn]);
                 }
@@ -392,8 +462,17 @@ struct DynLane {
         b_reg = Ev(C - 1);
         pg_c = pg_s = T(1);
         pg_p = T(0);
-        if constexpr (WANTZ)
-            q.load(C, cur);
+        if constexpr (WANTZ) {
+            if constexpr (CARRY_SMEM) {
+                for (int g = 0; g < Q_::G; ++g) {
+                    const typename Q_::V16 v = q.vec(C, g);
+                    scr[(2 * g) * ms] = v.a;
+                    scr[(2 * g + 1) * ms] = v.b;
+                }
+            } else {
+                q.load(C, cur);
+            }
+        }
         if constexpr (FASTQ) {
             da = sdl[C * ms];
             ia = sil[C * ms];
@@ -499,9 +578,14 @@ struct DynLane {
     __device__ __forceinline__ void renorm_carried()
     {
         if (scale_low(da)) {
+            if constexpr (CARRY_SMEM) {
+                for (int j = 0; j < NE; ++j)
+                    scr[j * ms] *= da;
+            } else {
 #pragma unroll
-            for (int j = 0; j < NE; ++j)
-                cur[j] *= da;
+                for (int j = 0; j < NE; ++j)
+                    cur[j] *= da;
+            }
             da = T(1);
             ia = T(1);
         }
@@ -526,7 +610,7 @@ struct DynLane {
     // step_q_carry for double above n = 32: column C-1 is read four 16-byte
     // vectors at a time, the next group's reads issued before this group's
     // writes, so only the carried column and two groups are live in
-    // registers.
+    // registers (above n = 64 the carried column moves to shared memory).
     __device__ __forceinline__ void step_q_carry_chunked(T cs, T sn)
     {
         constexpr int G = Q_::G;
@@ -569,7 +653,7 @@ struct DynLane {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int j = 2 * (grp * K + k);
-                E u0 = cur[j], u1 = cur[j + 1];
+                E u0 = carry(j), u1 = carry(j + 1);
                 E v0 = nx[bsel][k].a, v1 = nx[bsel][k].b;
                 if constexpr (FASTQ) {
                     const E s10 = f1 ? v0 : u0, s20 = f1 ? u0 : v0;
@@ -583,8 +667,8 @@ struct DynLane {
                     El<T>::rot(u1, v1, rr);
                 }
                 q.vec(C, grp * K + k) = V{u0, u1};
-                cur[j] = v0;
-                cur[j + 1] = v1;
+                carry(j) = v0;
+                carry(j + 1) = v1;
             }
         }
         if constexpr (FASTQ) {
@@ -597,7 +681,7 @@ struct DynLane {
             // end of the sweep: the carried column is final
 #pragma unroll
             for (int g = 0; g < G; ++g)
-                q.vec(C - 1, g) = V{cur[2 * g], cur[2 * g + 1]};
+                q.vec(C - 1, g) = V{carry(2 * g), carry(2 * g + 1)};
             if constexpr (FASTQ) {
                 sdl[(C - 1) * ms] = db2;
                 sil[(C - 1) * ms] = ib2;
@@ -700,6 +784,14 @@ __device__ __forceinline__ void dyn_body(const KParams &p)
     L.se = L.sd + NM * tpb;
     L.sdl = L.se + NM * tpb;
     L.sil = L.sdl + NM * tpb;
+    // The carried column above n = 64 (CARRY_SMEM): its own region after d
+    // and e (and, for double, the column scales), NE elements of the update's
+    // element type per thread, element j of thread t at [j * tpb + t].  The
+    // region starts at a multiple of 8 bytes from the shared base (sizes are
+    // whole NM * tpb arrays of T), so 8-byte elements stay aligned.
+    L.scr = reinterpret_cast<typename LaneT::E *>(reinterpret_cast<char *>(smem_raw) +
+                                                  size_t(LaneT::FASTQ ? 4 : 2) * NM * tpb * sizeof(T)) +
+            threadIdx.x;
     L.da = L.ia = T(1);
     L.pg = p.scheme == 1;
     if constexpr (WANTZ) {

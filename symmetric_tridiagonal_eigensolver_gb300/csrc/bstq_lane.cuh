@@ -305,27 +305,6 @@ struct QMix {
                 cur[j] = nx[j];
         }
     }
-    // Column s (static s in an unrolled loop) straight to global memory at
-    // qc: the register rows and the memory rows go out as separate 16-byte
-    // vectors, so no whole-column temporary is live beside the register
-    // rows.  Needs 16-byte aligned columns of exactly RR + MR rows.
-    __device__ __forceinline__ void store_col_direct(int s, T *qc) const
-    {
-        static_assert(NER % 2 == 0, "register rows in whole 16-byte vectors");
-        V16 *dst = reinterpret_cast<V16 *>(qc);
-#pragma unroll
-        for (int k = 0; k < NM; ++k)
-            if (k == s) {
-#pragma unroll
-                for (int v = 0; v < NER / 2; ++v)
-                    dst[v] = V16{qr[k][2 * v], qr[k][2 * v + 1]};
-            }
-        if constexpr (NEM > 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-                dst[NER / 2 + g] = base[vidx(s, g)];
-        }
-    }
     // Column s (static s in an unrolled loop), all stored rows, into out[].
     __device__ __forceinline__ void get_col(int s, T (&out)[RR + MR])
     {
@@ -833,6 +812,14 @@ struct Lane {
         jtot += two ? 0 : 1;
         f0 = dm - mu;
         g0 = gm;
+        if constexpr (sizeof(T) == 4) {
+            // float: the 2x2 solve runs as a one-position sweep seeded with
+            // its own rotation, lartg(cs2, sn2) = (cs2, sn2) to rounding, so
+            // the chase needs no separate 2x2 path; e_lo is set to zero
+            // through the mask when the pass is done (post_pass)
+            f0 = two ? cs2 : f0;
+            g0 = two ? sn2 : g0;
+        }
         m = mm;
         task = two ? TASK_2X2 : TASK_SWEEP;
     }
@@ -857,7 +844,7 @@ struct Lane {
         const unsigned upto = hi_l >= 31 ? ~0u : ((2u << hi_l) - 1u);  // bits 0..hi_l
         m_in = upto & (~0u << lo_l);
         m_touch = upto & (~0u << lo);
-        if (task == TASK_2X2) {
+        if (task == TASK_2X2 && sizeof(T) == 8) {
             m_act = 0u;
             m_22 = m_in;
             m_first = 0u;
@@ -923,10 +910,10 @@ struct Lane {
         if constexpr (DEFER)
             finish_at<C + 1>();
         const bool act = (m_act >> C) & 1u;
-        const bool a22 = (m_22 >> C) & 1u;
         const bool first = (m_first >> C) & 1u;
         // one select on the chain: the running pair, or the sweep's seed at
-        // its first position, or (1, 0) where the lane has no rotation
+        // its first position, or (1, 0) where the lane has no rotation (a
+        // 2x2 solve is a one-position sweep seeded with its rotation)
         const bool own = act && !first;
         const float fa = own ? f : (first ? f0 : 1.0f);
         const float ga = own ? g : (first ? g0 : 0.0f);
@@ -941,10 +928,9 @@ struct Lane {
         const float ee = fmaf(-r2, z2, 1.0f);  // 1 - r2 y0^2
         const float y = fmaf(0.5f * y0, ee, y0);  // 1/sqrt(r2), one Newton step
         const bool z = ga == 0.0f;
-        const bool idn = z && !a22;
-        float cs = fs * y, sn = gs * y;
-        cs = a22 ? cs2 : (z ? 1.0f : cs);
-        sn = a22 ? sn2 : sn;
+        float cs = fs * y;
+        const float sn = gs * y;
+        cs = z ? 1.0f : cs;
         const float a = d[C], b = e[C - 1], cc = d[C - 1];
         // e+ from 1/r2 (the chain), exactly e where g = 0
         const float d1 = fmaf(fs, fs, -gg);
@@ -957,9 +943,9 @@ struct Lane {
         const float p2 = fmaf(cs, b, sn * cc);
         const float dn = fmaf(cs, p1, sn * p2);
         d[C] = dn;
-        d[C - 1] = idn ? cc : (a + cc) - dn;
+        d[C - 1] = z ? cc : (a + cc) - dn;
         rpend = fmaf(fa, cs, ga * sn);
-        e[C - 1] = a22 ? 0.0f : en;
+        e[C - 1] = en;
         if constexpr (C >= 2) {
             const float eo = e[C - 2];
             g = (gs * eo) * y;  // new bulge s e''

@@ -74,10 +74,10 @@ constexpr int split_reg_rows()
 // The shared rows use the block's fixed lane stride (32 lanes per live pair),
 // and each position's rotation is read one position ahead, before the
 // position's store, so neither shared-memory read waits behind a store.
-template <int NM, int KEXIT>
+template <int NM, int KEXIT,
+          class QM = QMix<float, NM, split_reg_rows<NM>(), NM - split_reg_rows<NM>(), 32 * kSplitLivePairs>>
 struct QApplier {
-    static constexpr int RR = split_reg_rows<NM>();
-    QMix<float, NM, RR, NM - RR, 32 * kSplitLivePairs> Q;
+    QM Q;
     const float2 *buf;
     float2 rn;  // rotation of the next position
 
@@ -286,20 +286,12 @@ __global__ void __launch_bounds__(32 * 2 * kSplitPairs, 1) split_kernel(KParams 
                     qout[i] = __int_as_float(0x7fffffff);
             } else {
                 const bool vec = q_vector_ok<float>(p.Q, n);
-                if (vec && n == NM) {
-                    // whole aligned columns: register and shared rows written
-                    // as they are held
 #pragma unroll
-                    for (int s = 0; s < NM; ++s)
-                        A.Q.store_col_direct(s, qout + (long long)hpos[s * 32 * P] * n);
-                } else {
-#pragma unroll
-                    for (int s = 0; s < NM; ++s) {
-                        if (s < n) {
-                            float col[NM];
-                            A.Q.get_col(s, col);
-                            store_col(qout + (long long)hpos[s * 32 * P] * n, col, n, vec);
-                        }
+                for (int s = 0; s < NM; ++s) {
+                    if (s < n) {
+                        float col[NM];
+                        A.Q.get_col(s, col);
+                        store_col(qout + (long long)hpos[s * 32 * P] * n, col, n, vec);
                     }
                 }
             }

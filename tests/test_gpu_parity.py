@@ -166,9 +166,25 @@ def test_unsorted_output_order(dt):
 
 @pytest.mark.parametrize("dt", [F32, F64])
 @pytest.mark.parametrize("jobz", [True, False])
-@pytest.mark.parametrize("n", [33, 40, 48, 49, 57, 64])
+@pytest.mark.parametrize("n", [33, 40, 48, 49, 57, 64, 65, 80, 96, 97, 127, 128])
 def test_beyond_32(dt, n, jobz):
-    _case(dt, n, 2000 + 3 * n, jobz=jobz, seed=200 + n)
+    _case(dt, n, (2000 + 3 * n) if n <= 64 else 700 + n, jobz=jobz, seed=200 + n)
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_mixed_hard_cases_n128(dt):
+    """The mixed hard classes at the largest size, with the class checks."""
+    n, batch = 128, 700
+    d, e, labels, ab = inputs.mixed_problems(n, batch, dt, seed=2)
+    ref = oracle_ref(d, e, jobz=True)
+    lam, Q, info = run_gpu(d, e, jobz=True)
+    check_parity(d, e, lam, Q, info, ref, what=f"mixed n=128 {np.dtype(dt).name}")
+    z = labels == inputs.CLASS_INDEX["zero"]
+    assert np.all(lam[z] == 0) and np.all(Q[z] == np.eye(n, dtype=dt))
+    tn = H.norm1(d, e).astype(np.float64)
+    for b in np.nonzero(labels == inputs.CLASS_INDEX["toeplitz"])[0][:20]:
+        cf = H.toeplitz_eigenvalues(n, d[b, 0], e[b, 0]).astype(np.float64)
+        assert np.max(np.abs(lam[b] - cf)) <= H.lam_tol(n, dt, tn[b])
 
 
 @pytest.mark.parametrize("dt", [F32, F64])

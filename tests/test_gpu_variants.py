@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 
 from symmetric_tridiagonal_eigensolver_gb300 import inputs
+from tests import helpers as H
 from tests.gpu_helpers import check_parity, oracle_ref, run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -127,11 +128,12 @@ def test_dynamic_family_budget_and_poison(dt):
     assert np.all(info[ok] > 0) and np.mean(info[ok] == ref.info[ok]) > 0.9
 
 
-@pytest.mark.parametrize("n", [9, 12, 13, 16])
+@pytest.mark.parametrize("n", [9, 12, 13, 16, 17, 21, 24, 25, 29, 32])
 def test_split_role_kernel(n):
     """Chase warps record rotations, partner warps apply them to Q one pass
-    behind: same per-problem arithmetic as the static kernel, so equal
-    eigenvalues, and eigenvectors within the parity bounds."""
+    behind (above n = 16 several Q warps share a problem's rows): same
+    per-problem arithmetic as the static kernel, so equal eigenvalues, and
+    eigenvectors within the parity bounds."""
     d, e, _, _ = inputs.mixed_problems(n, 3333, np.float32, seed=90 + n)
     ref = oracle_ref(d, e)
     a = run_gpu(d, e, qstore=5)
@@ -147,11 +149,13 @@ def test_split_role_kernel(n):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("dt,n,params", [(np.float32, 16, {}), (np.float32, 16, {"qstore": 4}),
-                                         (np.float32, 8, {}), (np.float64, 12, {})])
+                                         (np.float32, 8, {}), (np.float64, 12, {}), (np.float32, 13, {}),
+                                         (np.float32, 7, {}), (np.float32, 27, {}), (np.float64, 3, {})])
 def test_unaligned_q_matches_aligned(dt, n, params):
     """Q columns go out in 16-byte vectors when Q starts on a 16-byte boundary
-    and n * sizeof(T) is a multiple of 16; a Q that is only element-aligned
-    takes the element-wise stores and must give the same bytes."""
+    and n * sizeof(T) is a multiple of 16; otherwise (a Q that is only
+    element-aligned, or a ragged n) the warp stages its columns and writes
+    them together.  Both must give the same bytes."""
     import torch
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
     d, e = inputs.normal_problems(n, 1000, dt, seed=21)
@@ -299,3 +303,33 @@ def test_pg_and_exp_agree_on_the_gpu():
     from tests import helpers as H
     tn = H.norm1(d, e).astype(np.float64)
     assert np.all(np.abs(a[0] - b[0]).max(1) <= 2 * H.lam_tol(12, np.float64, tn))
+
+
+@pytest.mark.parametrize("n", [20, 32])
+def test_split_role_rows_over_several_warps_back_transform_and_unaligned(n):
+    """Q warps that each hold a block of rows: the caller's basis enters row
+    block by row block (back_transform), and an element-aligned Q takes the
+    element path with the same bytes."""
+    import torch
+    from symmetric_tridiagonal_eigensolver_gb300 import bstq
+    dt = np.float32
+    batch = 1500
+    d, e = inputs.normal_problems(n, batch, dt, seed=400 + n)
+    Z = inputs.orthogonal_bases(n, batch, dt, seed=401 + n)
+    dev = torch.device("cuda:0")
+    lam, V, info = bstq.solve(torch.from_numpy(d.copy()).to(dev), torch.from_numpy(e.copy()).to(dev), jobz=True,
+                              Z=torch.from_numpy(Z).to(dev), qstore=5)
+    torch.cuda.synchronize()
+    lam, V = lam.cpu().numpy(), V.cpu().numpy()
+    res, orth = H.back_residual_orth(d, e, Z, lam, V)
+    tn = H.norm1(d, e).astype(np.float64)
+    eps = H.eps_of(dt)
+    assert np.all(res <= 64 * n * eps * tn) and np.all(orth <= 64 * n * eps)
+    ref = run_gpu(d, e, qstore=5)
+    buf = torch.full((batch * n * n + 1,), float("nan"), dtype=torch.float32, device=dev)
+    Qu = buf[1:].view(batch, n, n)
+    lam2, Q2, info2 = bstq.solve(torch.from_numpy(d.copy()).to(dev), torch.from_numpy(e.copy()).to(dev), jobz=True,
+                                 Q=Qu, qstore=5)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(Q2.cpu().numpy(), ref[1])
+    np.testing.assert_array_equal(lam2.cpu().numpy(), ref[0])

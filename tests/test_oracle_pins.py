@@ -116,6 +116,26 @@ def test_against_library_eigh_all_n(dt):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("n", [40, 64, 65, 96, 127, 128])
+def test_against_library_eigh_large_n(dt, n):
+    """Sizes above the sub-group width, up to the oracle's largest (128)."""
+    d, e = inputs.normal_problems(n, 12, dt, seed=500 + n)
+    r = oracle.steqr(d, e, jobz=True)
+    assert np.all(r.info == 0)
+    tn = H.norm1(d, e)
+    ref = np.linalg.eigvalsh(H.dense(d, e))
+    assert np.all(np.abs(r.lam.astype(np.float64) - ref).max(axis=1) <= H.lam_tol(n, dt, tn))
+    res, orth = H.residual_orth(d, e, r.lam, r.Q)
+    assert np.all(res <= 64 * n * H.eps_of(dt) * tn) and np.all(orth <= 64 * n * H.eps_of(dt))
+    # Toeplitz closed form at the same size
+    cf = H.toeplitz_eigenvalues(n, 0.5, -1.25)
+    rt = oracle.steqr(np.full((1, n), 0.5, dt), np.full((1, n - 1), -1.25, dt), jobz=False)
+    assert np.max(np.abs(rt.lam[0] - cf)) <= H.lam_tol(n, dt, 0.5 + 2.5)
+    with pytest.raises(ValueError):
+        oracle.steqr(np.zeros((1, 129), dt), np.zeros((1, 128), dt))
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 def test_trace_and_frobenius_invariants(dt):
     n = 20
     d, e = inputs.normal_problems(n, 200, dt, seed=3)
