@@ -63,19 +63,35 @@ NCU_TRAFFIC = {
 HEADLINE_UNIT = "bstq_kern_split_f32_v16.cu"
 
 
+def _source_dirs():
+    """Hand-written CUDA sources and the generated instantiation units (the
+    build writes those; they are regenerated here if missing)."""
+    from symmetric_tridiagonal_eigensolver_gb300 import build as _b
+    if not os.path.exists(os.path.join(_b.GEN, "bstq_registry_list.inc")):
+        _b.generate()
+    return [_b.CSRC, _b.GEN]
+
+
+def _find_source(f):
+    for d in _source_dirs():
+        if os.path.exists(os.path.join(d, f)):
+            return os.path.join(d, f)
+    return None
+
+
 def kernel_sources(unit: str = HEADLINE_UNIT) -> list:
     """The CUDA sources a kernel's translation unit compiles: the unit and
     every header it includes with quotes, followed recursively; names in
     order."""
     import re
-    csrc = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300", "csrc")
     seen, todo = set(), [unit]
     while todo:
         f = todo.pop()
-        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+        path = _find_source(f)
+        if f in seen or path is None:
             continue
         seen.add(f)
-        with open(os.path.join(csrc, f)) as fh:
+        with open(path) as fh:
             todo.extend(re.findall(r'^\s*#\s*include\s+"([^"]+)"', fh.read(), flags=re.M))
     return sorted(seen)
 
@@ -85,11 +101,10 @@ def kernel_digest(unit: str = HEADLINE_UNIT) -> str:
     shape, registers and shared memory are in bstq_describe()'s text, the
     other half of the traffic key."""
     import hashlib
-    csrc = os.path.join(ROOT, "symmetric_tridiagonal_eigensolver_gb300", "csrc")
     h = hashlib.sha256()
     for f in kernel_sources(unit):
         h.update(f.encode())
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(_find_source(f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

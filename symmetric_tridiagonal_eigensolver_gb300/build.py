@@ -15,11 +15,21 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
+GEN = os.path.join(BUILD, "gen")  # generated instantiation units
 LIB = os.path.join(HERE, "libbstq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, "-I", GEN]
+
+
+def generate() -> list:
+    """Write the kernel instantiation units (one per compiled variant) and
+    the registry list into _build/gen; returns their paths."""
+    if CSRC not in sys.path:
+        sys.path.insert(0, CSRC)
+    import gen_instances
+    return [os.path.join(GEN, f) for f in gen_instances.generate(GEN)]
 
 
 def _nvcc() -> str:
@@ -30,11 +40,14 @@ def _nvcc() -> str:
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    """The hand-written translation units and the generated ones."""
+    hand = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return hand + sorted(generate())
 
 
 def _headers():
     out = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h", ".inc"))]
+    out.append(os.path.join(GEN, "bstq_registry_list.inc"))
     out.append(os.path.join(INCLUDE, "bstq.h"))
     return out
 
@@ -50,8 +63,8 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
     """Compile every CUDA source and link libbstq.so; returns its path."""
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    hdrs = _headers()
     srcs = sources()
+    hdrs = _headers()
     objs = []
     todo = []
     for s in srcs:
