@@ -302,7 +302,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     } else {
         // d and e in shared memory, plus the column scales of the factored
         // double eigenvector update
-        smem_per_thread = 2 * size_t(nm) * elem + ((dtype == BSTQ_F64 && jobz) ? 2 * size_t(nm) * elem : 0);
+        smem_per_thread = 2 * size_t(nm) * elem + ((dtype == BSTQ_F64 && jobz && nm < 48) ? 2 * size_t(nm) * elem : 0);
         // the carried eigenvector column above n = 64
         if (jobz && nm > 64)
             smem_per_thread += size_t(nm) * elem;
@@ -341,6 +341,9 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
     pl.smem = smem_per_thread * tpb;
     pl.qwork_bytes = (qs == QS_GLOBAL) ? size_t(pl.grid) * mem_per_thread * tpb : 0;
+    // from n = 48 on, the double column scales follow Q in the scratch
+    if (family != FAMILY_STATIC && dtype == BSTQ_F64 && jobz && nm >= 48)
+        pl.qwork_bytes += size_t(pl.grid) * tpb * 2 * nm * elem;
     pl.work_bytes = align256(size_t(batch) * 4) + pl.qwork_bytes;
     if (pl.work_bytes == 0)
         pl.work_bytes = 256;

@@ -177,6 +177,11 @@ struct DynLane {
     // (f64 n = 64 V 169 against 221 ms, n = 48 45 against 77 ms): the extra
     // shared memory per thread cost a warp of occupancy.
     static constexpr bool CARRY_SMEM = NM > 64;
+    // From n = 48 on, the double column scales live in global scratch next
+    // to Q (element j of thread t at [j * blockDim + t], L1-resident)
+    // instead of shared memory: shared memory per thread, not registers,
+    // limited these kernels to three warps per SM.
+    static constexpr bool DELTA_GLOBAL = FASTQ && NM >= 48;
 
     T *sd, *se;  // this lane's d and e in shared memory
     T *sdl, *sil;  // column scales delta_j and 1/delta_j (FASTQ)
@@ -784,13 +789,23 @@ __device__ __forceinline__ void dyn_body(const KParams &p)
     L.se = L.sd + NM * tpb;
     L.sdl = L.se + NM * tpb;
     L.sil = L.sdl + NM * tpb;
+    if constexpr (LaneT::DELTA_GLOBAL) {
+        // the column scales after every block's Q scratch, per block 2 NM
+        // arrays of tpb values
+        T *dg = reinterpret_cast<T *>(reinterpret_cast<typename DynQ<T, NM>::V16 *>(p.qwork) +
+                                      (long long)gridDim.x * NM * DynQ<T, NM>::G * tpb);
+        L.sdl = dg + (long long)blockIdx.x * 2 * NM * tpb + threadIdx.x;
+        L.sil = L.sdl + NM * tpb;
+    }
     // The carried column above n = 64 (CARRY_SMEM): its own region after d
-    // and e (and, for double, the column scales), NE elements of the update's
-    // element type per thread, element j of thread t at [j * tpb + t].  The
-    // region starts at a multiple of 8 bytes from the shared base (sizes are
-    // whole NM * tpb arrays of T), so 8-byte elements stay aligned.
-    L.scr = reinterpret_cast<typename LaneT::E *>(reinterpret_cast<char *>(smem_raw) +
-                                                  size_t(LaneT::FASTQ ? 4 : 2) * NM * tpb * sizeof(T)) +
+    // and e (and the column scales when they are in shared memory), NE
+    // elements of the update's element type per thread, element j of thread
+    // t at [j * tpb + t].  The region starts at a multiple of 8 bytes from
+    // the shared base (sizes are whole NM * tpb arrays of T), so 8-byte
+    // elements stay aligned.
+    L.scr = reinterpret_cast<typename LaneT::E *>(
+                reinterpret_cast<char *>(smem_raw) +
+                size_t((LaneT::FASTQ && !LaneT::DELTA_GLOBAL) ? 4 : 2) * NM * tpb * sizeof(T)) +
             threadIdx.x;
     L.da = L.ia = T(1);
     L.pg = p.scheme == 1;

@@ -796,7 +796,8 @@ struct Lane {
         const T dm = mir_d(mm), gm = mir_e(mm - 1);
         T t, mu;
         shift_tangent(d1, d2, e1, t, mu);
-        rot_from_tangent(t, cs2, sn2);  // used by a 2x2 solve only
+        if constexpr (sizeof(T) == 8)
+            rot_from_tangent(t, cs2, sn2);  // used by a 2x2 solve only
         const bool two = mm == lo + 1;  // 2x2 direct solve, applied in the next pass
         if (!two && jtot == budget) {  // sweep budget exhausted
             unscale_block(true);
@@ -814,11 +815,13 @@ struct Lane {
         g0 = gm;
         if constexpr (sizeof(T) == 4) {
             // float: the 2x2 solve runs as a one-position sweep seeded with
-            // its own rotation, lartg(cs2, sn2) = (cs2, sn2) to rounding, so
-            // the chase needs no separate 2x2 path; e_lo is set to zero
-            // through the mask when the pass is done (post_pass)
-            f0 = two ? cs2 : f0;
-            g0 = two ? sn2 : g0;
+            // the direction (1, t) of its rotation: lartg(1, t) is
+            // (1, t) / sqrt(1 + t^2), the rotation with tangent t, so the
+            // chase needs no separate 2x2 path and the settle step no
+            // second square root; e_lo is set to zero through the mask when
+            // the pass is done (post_pass)
+            f0 = two ? T(1) : f0;
+            g0 = two ? t : g0;
         }
         m = mm;
         task = two ? TASK_2X2 : TASK_SWEEP;
