@@ -68,8 +68,13 @@ typedef enum {
     BSTQ_QSTORE_SHARED = 2,    /* per-lane columns in shared memory      */
     BSTQ_QSTORE_GLOBAL = 3,    /* per-lane columns in `work` (L1/L2)     */
     BSTQ_QSTORE_HYBRID = 4,    /* 8 rows in registers, rest in shared    */
-    BSTQ_QSTORE_SPLIT = 5      /* float, n <= 16: separate warps apply the
+    BSTQ_QSTORE_SPLIT = 5,     /* float, n <= 32: separate warps apply the
                                   rotations to Q held in their registers */
+    BSTQ_QSTORE_LOG = 6        /* float, n > 32, flat scheduler (the
+                                  default there): each lane logs its
+                                  problem's rotations in `work`; the warp
+                                  then applies each log to Q rows held in
+                                  registers (record and apply) */
 } bstq_qstore;
 
 /* Options; an all-zero struct means the defaults. */
@@ -91,6 +96,13 @@ typedef struct {
                               with lambda (BatchLAS page "algo_steqr",
                               eigenvector accumulation: back_transform).     */
     int update_scheme;     /* bstq_update_scheme: 0 (default) EXP, 1 PG.    */
+    int log_entries;       /* BSTQ_QSTORE_LOG only: rotation log entries per
+                              problem (8 bytes each, in `work`), rounded up
+                              to whole pages of 256; 0 = 1.5 n^2 + 8n, which
+                              holds a typical solve in one apply round.  A
+                              smaller log needs less workspace and costs
+                              more rounds (Q goes through global memory once
+                              per round); negative values return -10.       */
 } bstq_params;
 
 /* Form of the implicit step (BatchLAS page "algo_steqr", update schemes).

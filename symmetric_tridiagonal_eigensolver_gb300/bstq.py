@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libbstq.so")
 F32, F64 = 0, 1
 JOBZ_N, JOBZ_V = 0, 1
 SCHED_AUTO, SCHED_FLAT, SCHED_NESTED = 0, 1, 2
-QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID, QSTORE_SPLIT = 0, 1, 2, 3, 4, 5
+QSTORE_AUTO, QSTORE_REGISTERS, QSTORE_SHARED, QSTORE_GLOBAL, QSTORE_HYBRID, QSTORE_SPLIT, QSTORE_LOG = 0, 1, 2, 3, 4, 5, 6
 KERNEL_AUTO, KERNEL_STATIC, KERNEL_DYNAMIC = 0, 1, 2
 UPDATE_EXP, UPDATE_PG = 0, 1
 ERR_CUDA, ERR_NODEVICE = 1, 2
@@ -47,7 +47,8 @@ class Params(ctypes.Structure):
     _fields_ = [("no_sort", ctypes.c_int), ("max_sweeps_per_n", ctypes.c_int),
                 ("scheduler", ctypes.c_int), ("qstore", ctypes.c_int),
                 ("threads_per_block", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("back_transform", ctypes.c_int), ("update_scheme", ctypes.c_int)]
+                ("back_transform", ctypes.c_int), ("update_scheme", ctypes.c_int),
+                ("log_entries", ctypes.c_int)]
 
 
 class BstqError(RuntimeError):
@@ -118,11 +119,12 @@ def load(path: str = LIB_PATH):
 
 
 def _params(no_sort=False, max_sweeps_per_n=0, scheduler=0, qstore=0, threads_per_block=0, kernel=0,
-            back_transform=False, update_scheme=0):
+            back_transform=False, update_scheme=0, log_entries=0):
     if isinstance(update_scheme, str):
         update_scheme = {"exp": UPDATE_EXP, "pg": UPDATE_PG}[update_scheme.lower()]
     return Params(int(bool(no_sort)), int(max_sweeps_per_n), int(scheduler), int(qstore),
-                  int(threads_per_block), int(kernel), int(bool(back_transform)), int(update_scheme))
+                  int(threads_per_block), int(kernel), int(bool(back_transform)), int(update_scheme),
+                  int(log_entries))
 
 
 def _dtype_code(dt) -> int:

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/bstq.h"
+#include "bstq_rlog.cuh"
 #include "bstq_split2.cuh"
 #include "bstq_diag.h"
 #include "bstq_leaves.h"
@@ -25,7 +26,14 @@ struct Plan {
     size_t smem = 0;
     size_t qwork_bytes = 0;
     size_t work_bytes = 0;
-    int ppb = 0;  // problems per block (split-role kernel)
+    int ppb = 0;  // problems per block (split-role kernel) or per warp (record-and-apply)
+    // record-and-apply: log entries per problem, the apply and finishing
+    // launches, and the offsets of the log lengths, maps and logs in work
+    long long lcap = 0;
+    int tpb2 = 0, tpb3 = 0;
+    long long grid2 = 0, grid3 = 0;
+    size_t smem2 = 0, smem3 = 0;
+    size_t off_cnt = 0, off_map = 0, off_log = 0;
 };
 
 constexpr int kNmList[] = {4, 8, 12, 16, 24, 32, 48, 64, 96, 128};
@@ -110,10 +118,15 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched, in
 //     in registers, the rest streamed from shared memory (one wave of 32768
 //     problems stays resident);
 //   double: registers for n <= 8, else global scratch (its FP64 pipe, not
-//     L1/L2, bounds it).
+//     L1/L2, bounds it);
+//   float n > 32, flat scheduler: the record-and-apply kernel
+//     (bstq_rlog.cuh); under the nested scheduler the dynamic-position
+//     kernel with Q in global scratch.
 int default_qstore(int dtype, int nm, int sched)
 {
     if (dtype == 0) {
+        if (nm > 32 && sched == SCHED_FLAT)
+            return QS_LOG;
         if (nm <= 8)
             return QS_REG;
         if (nm <= 32 && sched == SCHED_FLAT)
@@ -192,7 +205,9 @@ int check_args(int dtype, int jobz, int n, long long batch, const bstq_params *p
             return -10;
         if (p->scheduler < 0 || p->scheduler > 2)
             return -10;
-        if (p->qstore < 0 || p->qstore > 5)
+        if (p->qstore < 0 || p->qstore > 6)
+            return -10;
+        if (p->log_entries < 0)
             return -10;
         if (p->kernel < 0 || p->kernel > 2)
             return -10;
@@ -228,7 +243,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     if (pg && family == FAMILY_STATIC)
         return -10;  // the PG step runs in the dynamic-position kernels only
     int qs = jobz ? ((p && p->qstore) ? p->qstore : default_qstore(dtype, nm, sched)) : 0;
-    if (family != FAMILY_STATIC && jobz)
+    if (family != FAMILY_STATIC && jobz && qs != QS_LOG)
         qs = QS_GLOBAL;  // the dynamic kernels keep Q in global scratch
     pl.k = find_entry(dtype, jobz, nm, qs, sched, family);
     if (!pl.k)
@@ -237,6 +252,67 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
     if (cudaFuncGetAttributes(&fa, pl.k->fn) != cudaSuccess) {
         cudaGetLastError();
         return BSTQ_ERR_NODEVICE;
+    }
+    if (qs == QS_LOG) {
+        // record-and-apply (bstq_rlog.cuh), three launches:
+        //  chase: one problem per thread, d and e in shared memory, blocks
+        //    as the dynamic-position kernel's (threads_per_block applies);
+        //  apply: one warp per problem and row chunk, four warps per block;
+        //  finish: two warps of 32 problem slots per block, for the
+        //    problems whose log ran out of room (normally none).
+        // The log holds whole pages (a pass never crosses a page).
+        // default: 1.5 n^2 + 8 n entries; a solve takes about n^2 entries
+        // of rotations and headers (N(0,1) input) and the page ends waste
+        // up to n / 2 per page on average
+        const long long want = (p && p->log_entries) ? p->log_entries : 3LL * n * n / 2 + 8LL * n;
+        const long long lcap = (want + kRlogPage - 1) / kRlogPage * kRlogPage;
+        const size_t per_thread = 2 * size_t(nm) * 4;
+        const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
+        int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);
+        cap = cap / 32 * 32;
+        if (cap > di.max_threads_sm)
+            cap = di.max_threads_sm;
+        const int by_smem = (int)((size_t)di.max_smem_block / per_thread) / 32 * 32;
+        if (by_smem < cap)
+            cap = by_smem;
+        if (cap > fa.maxThreadsPerBlock)
+            cap = fa.maxThreadsPerBlock / 32 * 32;
+        if (cap > 1024)
+            cap = 1024;
+        if (cap < 32)
+            return -10;
+        int tpb;
+        if (p && p->threads_per_block) {
+            tpb = p->threads_per_block;
+            if (tpb > cap)
+                return -10;
+        } else {
+            tpb = choose_block_size(batch, di.sms, cap, false);
+        }
+        pl.tpb = tpb;
+        pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
+        pl.smem = per_thread * tpb;
+        const int rows = nm <= 64 ? 64 : 32;
+        const long long chunks = (n + rows - 1) / rows;
+        constexpr int kApplyWarps = 4;
+        pl.tpb2 = 32 * kApplyWarps;
+        pl.smem2 = size_t(kApplyWarps) * Rlog<64>::WARP_BYTES;
+        pl.grid2 = batch > 0 ? (batch * chunks + kApplyWarps - 1) / kApplyWarps : 0;
+        pl.tpb3 = 64;
+        pl.ppb = 32;
+        pl.smem3 = rlog_smem_bytes(nm, 2, 32);
+        pl.grid3 = batch > 0 ? (batch + 63) / 64 : 0;
+        if (pl.smem2 > (size_t)di.max_smem_block || pl.smem3 > (size_t)di.max_smem_block)
+            return -10;
+        pl.lcap = lcap;
+        pl.off_cnt = align256(size_t(batch) * 4);
+        pl.off_map = pl.off_cnt + align256(size_t(batch) * 4);
+        pl.off_log = pl.off_map + align256(size_t(batch) * 2 * size_t(n));
+        pl.qwork_bytes = size_t(batch) * size_t(lcap) * sizeof(float2);
+        pl.work_bytes = pl.off_log + pl.qwork_bytes;
+        if (pl.work_bytes < 256)
+            pl.work_bytes = 256;
+        return 0;
     }
     if (qs == QS_SPLIT && (nm == 24 || nm == 32)) {
         // several Q warps per chase warp (bstq_split2.cuh): fixed block
@@ -358,6 +434,7 @@ const char *qs_name(int qs)
     case QS_GLOBAL: return "global";
     case QS_HYBRID: return "hybrid";
     case QS_SPLIT: return "split";
+    case QS_LOG: return "log";
     default: return "none";
     }
 }
@@ -380,12 +457,42 @@ int launch(const Plan &pl, int n, long long batch, int dtype, void *d, const voi
     kp.back = (Q && p && p->back_transform) ? 1 : 0;
     kp.scheme = (p && p->update_scheme) ? 1 : 0;
     (void)dtype;
+    void *args[] = {&kp};
+    if (pl.k->qs == QS_LOG) {
+        // record-and-apply: chase, apply, finish
+        char *w = reinterpret_cast<char *>(work);
+        kp.lcnt = reinterpret_cast<int *>(w + pl.off_cnt);
+        kp.lmap = reinterpret_cast<unsigned char *>(w + pl.off_map);
+        kp.qwork = w + pl.off_log;
+        kp.lcap = pl.lcap;
+        const void *fns[3] = {pl.k->fn, pl.k->fn2, pl.k->fn3};
+        const long long grids[3] = {pl.grid, pl.grid2, pl.grid3};
+        const int tpbs[3] = {pl.tpb, pl.tpb2, pl.tpb3};
+        const size_t smems[3] = {pl.smem, pl.smem2, pl.smem3};
+        for (int i = 0; i < 3; ++i) {
+            if (!fns[i])
+                return -10;
+            if (grids[i] > 0x7fffffffLL)
+                return -4;
+        }
+        for (int i = 0; i < 3; ++i) {
+            if (smems[i] > 48 * 1024) {
+                cudaError_t err =
+                    cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smems[i]);
+                if (err != cudaSuccess)
+                    return cuda_fail(err, "cudaFuncSetAttribute");
+            }
+            cudaError_t err = cudaLaunchKernel(fns[i], dim3((unsigned)grids[i]), dim3(tpbs[i]), args, smems[i], st);
+            if (err != cudaSuccess)
+                return cuda_fail(err, "cudaLaunchKernel");
+        }
+        return 0;
+    }
     if (pl.smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(pl.k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (err != cudaSuccess)
             return cuda_fail(err, "cudaFuncSetAttribute");
     }
-    void *args[] = {&kp};
     if (pl.grid > 0x7fffffffLL)
         return -4;
     cudaError_t err = cudaLaunchKernel(pl.k->fn, dim3((unsigned)pl.grid), dim3(pl.tpb), args, pl.smem, st);

@@ -154,8 +154,13 @@ constexpr bool dyn_fastq()
     return WANTZ && sizeof(T) == 8;
 }
 
-template <typename T, int NM, bool WANTZ>
+// With LOG set (float, eigenvalues-only chase) every pass is also appended
+// to the problem's rotation log: a header entry (top position m, number of
+// rotations L, as integer bits) and then the rotations (cs, sn) of positions
+// m, m-1, ..., m-L+1 (the record-and-apply kernel, bstq_rlog.cuh).
+template <typename T, int NM, bool WANTZ, bool LOG = false>
 struct DynLane {
+    static_assert(!LOG || (sizeof(T) == 4 && !WANTZ), "the rotation log is for the float chase without Q");
     using C_ = Consts<T>;
     using Q_ = DynQ<T, NM>;
     using E = typename Q_::E;
@@ -206,6 +211,8 @@ struct DynLane {
     E cur[CARRY_SMEM ? 1 : NE];  // Q column C (the column shared with the next rotation)
     E *scr;        // CARRY_SMEM: that column in shared memory instead,
                    // element j at scr[j * ms]
+    float2 *lg;    // LOG: this problem's rotation log and its entry count
+    int cnt;
     __device__ __forceinline__ E &carry(int j)
     {
         if constexpr (CARRY_SMEM)
@@ -463,6 +470,8 @@ struct DynLane {
         }
         C = m;
         L = m - lo;  // 1 for a 2x2 task
+        if constexpr (LOG)
+            lg[cnt++] = make_float2(__int_as_float(m), __int_as_float(L));
         a_reg = D(C);
         b_reg = Ev(C - 1);
         pg_c = pg_s = T(1);
@@ -516,6 +525,8 @@ struct DynLane {
             step_exp(k, sweep, cs, sn, r);
         }
         step_q(cs, sn);
+        if constexpr (LOG)
+            lg[cnt++] = make_float2(cs, sn);
         --C;
     }
 

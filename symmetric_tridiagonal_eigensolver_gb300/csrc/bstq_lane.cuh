@@ -33,7 +33,7 @@
 
 namespace bstq {
 
-enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3, QS_HYBRID = 4, QS_SPLIT = 5 };
+enum { QS_REG = 1, QS_SMEM = 2, QS_GLOBAL = 3, QS_HYBRID = 4, QS_SPLIT = 5, QS_LOG = 6 };
 enum { SCHED_FLAT = 1, SCHED_NESTED = 2 };
 enum { ST_RUN = 0, ST_DONE = 1, ST_FAIL = 2, ST_BAD = 3, ST_DEAD = 4 };
 enum { TASK_NONE = 0, TASK_SWEEP = 1, TASK_2X2 = 2 };
@@ -57,6 +57,9 @@ struct KParams {
     int scheme;        // 0 EXP, 1 PG update (dynamic-position kernels)
     const void *A;     // fused syev: dense input, batch x n x n
     void *sscr;        // fused syev: the reduction's scratch
+    long long lcap;    // record-and-apply kernels: rotation log entries per problem,
+    int *lcnt;         // per problem log length (or a state code),
+    unsigned char *lmap;  // per problem column maps (2 n bytes)
 };
 
 // ---------------------------------------------------------------------------

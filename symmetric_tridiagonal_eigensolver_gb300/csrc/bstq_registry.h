@@ -15,6 +15,8 @@ struct KernelEntry {
     const void *fn;
     int family;  // FAMILY_STATIC (bstq_lane.cuh) / FAMILY_DYNAMIC (bstq_dyn.cuh) /
                  // FAMILY_SYEV (bstq_syev.cuh, fused dense solve)
+    const void *fn2 = nullptr;  // record-and-apply: the apply kernel
+    const void *fn3 = nullptr;  // record-and-apply: the finishing kernel
 };
 
 enum { FAMILY_STATIC = 1, FAMILY_DYNAMIC = 2, FAMILY_SYEV = 3 };

@@ -46,6 +46,9 @@ int main(int argc, char **argv)
     memset(&prm, 0, sizeof(prm));
     prm.scheduler = 9;
     expect("solve_ex params", bstq_solve_ex(BSTQ_F32, BSTQ_JOBZ_V, 8, 10, p, p, p, p, NULL, &prm), -10);
+    memset(&prm, 0, sizeof(prm));
+    prm.log_entries = -1;
+    expect("solve_ex log entries", bstq_solve_ex(BSTQ_F32, BSTQ_JOBZ_V, 64, 10, p, p, p, p, NULL, &prm), -10);
 
     expect("stedc_leaves leaf", bstq_stedc_leaves(BSTQ_F32, BSTQ_JOBZ_V, 70, 0, 10, p, p, p, (int32_t *)p, p,
                                                   NULL, NULL), -3);

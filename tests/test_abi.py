@@ -63,6 +63,8 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
     p = bstq.Params(0, 0, 0, 0, 48, 0)
     assert lib.bstq_solve_ex(0, 1, 8, 10, good, good, good, good, None, ctypes.byref(p)) == -10
+    p = bstq._params(log_entries=-1)   # rotation log capacity: checked before any device query
+    assert lib.bstq_solve_ex(0, 1, 64, 10, good, good, good, good, None, ctypes.byref(p)) == -10
     assert lib.bstq_work_size(0, 1, 40, 10) == 0
     assert lib.bstq_solve_host(0, 1, 8, 10, None, good, good, good, good, None, None) == -5
     # the diagnostic entry point
