@@ -155,9 +155,14 @@ constexpr bool dyn_fastq()
 }
 
 // With LOG set (float, eigenvalues-only chase) every pass is also appended
-// to the problem's rotation log: a header entry (top position m, number of
-// rotations L, as integer bits) and then the rotations (cs, sn) of positions
-// m, m-1, ..., m-L+1 (the record-and-apply kernel, bstq_rlog.cuh).
+// to the problem's rotation log (the record-and-apply kernels,
+// bstq_rlog.cuh): a header entry (top position m and count, as integer
+// bits), the rotations (cs, sn) of positions m, m-1, ..., lo + 1, and
+// identity rotations (1, 0) for positions lo, ..., down to the next
+// multiple of kRlogGroup, so that every logged pass ends on a group
+// boundary and its reader tests for the end once per group.
+constexpr int kRlogGroup = 4;
+
 template <typename T, int NM, bool WANTZ, bool LOG = false>
 struct DynLane {
     static_assert(!LOG || (sizeof(T) == 4 && !WANTZ), "the rotation log is for the float chase without Q");
@@ -211,8 +216,8 @@ struct DynLane {
     E cur[CARRY_SMEM ? 1 : NE];  // Q column C (the column shared with the next rotation)
     E *scr;        // CARRY_SMEM: that column in shared memory instead,
                    // element j at scr[j * ms]
-    float2 *lg;    // LOG: this problem's rotation log and its entry count
-    int cnt;
+    float2 *lg;    // LOG: this problem's rotation log, its entry count and
+    int cnt, lpad; // the identity entries that end the current pass
     __device__ __forceinline__ E &carry(int j)
     {
         if constexpr (CARRY_SMEM)
@@ -470,8 +475,13 @@ struct DynLane {
         }
         C = m;
         L = m - lo;  // 1 for a 2x2 task
-        if constexpr (LOG)
-            lg[cnt++] = make_float2(__int_as_float(m), __int_as_float(L));
+        if constexpr (LOG) {
+            lpad = lo % kRlogGroup;
+            lg[cnt] = make_float2(__int_as_float(m), __int_as_float(L + lpad));
+            for (int i = 0; i < lpad; ++i)
+                lg[cnt + 1 + L + i] = make_float2(1.f, 0.f);
+            ++cnt;
+        }
         a_reg = D(C);
         b_reg = Ev(C - 1);
         pg_c = pg_s = T(1);
@@ -772,6 +782,8 @@ struct DynLane {
 
     __device__ __forceinline__ void post_pass()
     {
+        if constexpr (LOG)
+            cnt += lpad;  // the identity entries written with the header
         if (task == TASK_2X2) {
             lo += 2;
             if (lo > le)

@@ -10,7 +10,9 @@
 //  1. rlog_chase_kernel: lane b runs the dynamic-position chase of problem b
 //     without Q and appends every pass to the problem's rotation log in
 //     global memory: a header (top position m, count L) and the rotations
-//     (cs, sn) of positions m, m-1, ..., m-L+1.  The log is cut into pages
+//     (cs, sn) of positions m, m-1, ..., m-L+1, the last few of them
+//     identities that end the pass on a multiple of kRlogGroup (bstq_dyn.cuh).
+//     The log is cut into pages
 //     of kRlogPage entries and a pass never crosses a page boundary: a pass
 //     that does not fit in the rest of a page starts the next page, after
 //     an end-of-page header (0, 0).  The lane writes the eigenvalues, info,
@@ -81,9 +83,11 @@ __device__ __forceinline__ void rlog_rot(float (&q)[RPL][NM], const float2 r)
     }
 }
 
-// One logged pass: positions m down to lo + 1.  top points at the entry of
-// position 0, so position C's rotation is top[-C].  The switch enters at m
-// and the pass leaves after position lo + 1.  Rotations are read two
+// One logged pass: positions m down to lo + 1, lo a multiple of
+// kRlogGroup.  top points at the entry of position 0, so position C's
+// rotation is top[-C].  The switch enters at m; the end test runs only at
+// group boundaries.  An identity rotation leaves the rows as they were
+// (up to the sign of a zero).  Rotations are read two
 // positions ahead into three slots indexed by position mod 3 (compile-time
 // indices, so the slots stay in registers); the reads past the pass's end
 // land in the two slack entries of the page and are not used.
@@ -110,8 +114,10 @@ __device__ __forceinline__ void rlog_pass(float (&q)[RPL][NM], const float2 *top
         if constexpr ((C) <= NM - 1) {                                        \
             sl[((C) + 1) % 3] = top[2 - (C)];                                 \
             rlog_rot<(C), NM, RPL>(q, sl[(C) % 3]);                           \
-            if ((C) - 1 <= lo)                                                \
-                break;                                                        \
+            if constexpr (((C) - 1) % kRlogGroup == 0) {                      \
+                if ((C) - 1 <= lo)                                            \
+                    break;                                                    \
+            }                                                                 \
         }
 #define BSTQ_RL8(B)                                                           \
     BSTQ_RL(B + 7) BSTQ_RL(B + 6) BSTQ_RL(B + 5) BSTQ_RL(B + 4) BSTQ_RL(B + 3) \
@@ -210,9 +216,10 @@ __device__ __forceinline__ void rlog_apply_rows(const float2 *lq, int cq, float 
         while (w < plen) {
             const float2 h = pg[w];
             const int m = __float_as_int(h.x), ls = __float_as_int(h.y);
-            // a pass is 1 <= ls <= m <= NM - 1 rotations, whole inside the
-            // page; an end-of-page header has ls = 0
-            if (ls < 1 || ls > m || m >= NM || w + 1 + ls > plen)
+            // a pass is 1 <= ls <= m <= NM - 1 rotations ending on a group
+            // boundary, whole inside the page; an end-of-page header has
+            // ls = 0
+            if (ls < 1 || ls > m || m >= NM || (m - ls) % kRlogGroup != 0 || w + 1 + ls > plen)
                 break;
             rlog_pass<NM, RPL>(q, pg + w + 1 + m, m, m - ls);
             w += 1 + ls;
@@ -290,6 +297,7 @@ __global__ void rlog_chase_kernel(KParams p)
     L.pg = p.scheme == 1;
     L.lg = reinterpret_cast<float2 *>(p.qwork) + (live ? b : 0) * cap;
     L.cnt = 0;
+    L.lpad = 0;
     L.load(p, b, live);
     unsigned char *mp = p.lmap + (live ? b : 0) * 2 * n;
     if (live && L.status == ST_RUN)
@@ -300,8 +308,8 @@ __global__ void rlog_chase_kernel(KParams p)
         if (L.status == ST_RUN && L.task == TASK_NONE)
             L.settle_step();
         bool has = L.has_task();
-        // a pass takes 1 + (m - lo) entries inside one page
-        const int need = 1 + (L.m - L.lo);
+        // a pass takes 1 + (m - lo) entries and its padding inside one page
+        const int need = 1 + L.m - (L.lo / kRlogGroup) * kRlogGroup;
         if (has) {
             long long at = L.cnt;
             if ((at % kRlogPage) + need > kRlogPage)
@@ -410,6 +418,7 @@ __global__ void __launch_bounds__(256, 1) rlog_kernel(KParams p)
     L.pg = p.scheme == 1;
     L.lg = reinterpret_cast<float2 *>(p.qwork) + (live ? b : 0) * cap;
     L.cnt = 0;
+    L.lpad = 0;
     L.load(p, b, live);
     if (live && L.status == ST_RUN)
         for (int s = 0; s < n; ++s)
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(256, 1) rlog_kernel(KParams p)
             break;
         // apply the logs first when one of the warp's lanes has no room left
         // for its pass
-        const int need = 1 + (L.m - L.lo);
+        const int need = 1 + L.m - (L.lo / kRlogGroup) * kRlogGroup;
         long long at = L.cnt;
         if (has && (at % kRlogPage) + need > kRlogPage)
             at = (at / kRlogPage + 1) * kRlogPage;

@@ -59,7 +59,9 @@ def test_log_capacity_changes_no_bit(n):
     them, unpermuted until the last round)."""
     d, e = inputs.normal_problems(n, 300, F32, seed=700 + n)
     ref = run_gpu(d, e, qstore=LOG)
-    for cap in (1, 300, 7 * n):   # whole pages of 256 entries: 1, 2 and 2-4 pages
+    # whole pages of 256 entries: every log runs out (1, 300, 7 n), or only
+    # some do (n^2: about the mean log length)
+    for cap in (1, 300, 7 * n, n * n):
         _same(run_gpu(d, e, qstore=LOG, log_entries=cap), ref, f"n={n} log_entries={cap}")
 
 
