@@ -292,7 +292,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         pl.tpb = tpb;
         pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
         pl.smem = per_thread * tpb;
-        const int rows = nm <= 64 ? 64 : 32;
+        const int rows = rlog_rows(nm);
         const long long chunks = (n + rows - 1) / rows;
         constexpr int kApplyWarps = 4;
         pl.tpb2 = 32 * kApplyWarps;

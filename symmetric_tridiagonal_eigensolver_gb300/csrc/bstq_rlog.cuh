@@ -43,6 +43,9 @@ namespace bstq {
 
 constexpr int kRlogPage = 256;  // log entries per page
 
+// Rows of Q one warp of the apply holds at once (Rlog<NM>::ROWS).
+__host__ __device__ constexpr int rlog_rows(int nm) { return (nm > 32 && nm <= 64) ? 64 : 32; }
+
 template <int NM>
 struct Rlog {
     // Rows of Q per lane: two for n <= 64 (rows r0 + lane and r0 + 32 +
@@ -50,8 +53,9 @@ struct Rlog {
     // on GB300 a packed f32x2 rotation (mul, then fma into the other row)
     // measured 23 cycles of latency against 8.4 for the scalar pair, and
     // the update is bound by that chain.
-    static constexpr int RPL = NM <= 64 ? 2 : 1;
+    static constexpr int RPL = (NM > 32 && NM <= 64) ? 2 : 1;
     static constexpr int ROWS = 32 * RPL;  // rows of Q a warp holds at once
+    static_assert(ROWS == rlog_rows(NM), "one rule for the rows per warp");
     // three page buffers per warp (pages k, k+1, k+2 in flight), each with
     // two entries of slack for the reads ahead
     static constexpr int BUF = kRlogPage + 2;
