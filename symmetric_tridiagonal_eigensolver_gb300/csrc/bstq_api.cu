@@ -261,11 +261,7 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         //  finish: two warps of 32 problem slots per block, for the
         //    problems whose log ran out of room (normally none).
         // The log holds whole pages (a pass never crosses a page).
-        // default: 1.5 n^2 + 8 n entries; a solve takes about n^2 entries
-        // of rotations and headers (N(0,1) input) and the page ends waste
-        // up to n / 2 per page on average
-        const long long want = (p && p->log_entries) ? p->log_entries : 3LL * n * n / 2 + 8LL * n;
-        const long long lcap = (want + kRlogPage - 1) / kRlogPage * kRlogPage;
+        const RlogLayout lay = rlog_layout(batch, n, nm, p ? p->log_entries : 0);
         const size_t per_thread = 2 * size_t(nm) * 4;
         const int regs = fa.numRegs > 0 ? fa.numRegs : 1;
         int cap = di.max_regs_sm / (((regs + 7) / 8) * 8);
@@ -292,26 +288,22 @@ int make_plan(int dtype, int jobz, int n, long long batch, const bstq_params *p,
         pl.tpb = tpb;
         pl.grid = batch > 0 ? (batch + tpb - 1) / tpb : 0;
         pl.smem = per_thread * tpb;
-        const int rows = rlog_rows(nm);
-        const long long chunks = (n + rows - 1) / rows;
         constexpr int kApplyWarps = 4;
         pl.tpb2 = 32 * kApplyWarps;
         pl.smem2 = size_t(kApplyWarps) * Rlog<64>::WARP_BYTES;
-        pl.grid2 = batch > 0 ? (batch * chunks + kApplyWarps - 1) / kApplyWarps : 0;
+        pl.grid2 = (lay.apply_warps + kApplyWarps - 1) / kApplyWarps;
         pl.tpb3 = 64;
         pl.ppb = 32;
         pl.smem3 = rlog_smem_bytes(nm, 2, 32);
         pl.grid3 = batch > 0 ? (batch + 63) / 64 : 0;
         if (pl.smem2 > (size_t)di.max_smem_block || pl.smem3 > (size_t)di.max_smem_block)
             return -10;
-        pl.lcap = lcap;
-        pl.off_cnt = align256(size_t(batch) * 4);
-        pl.off_map = pl.off_cnt + align256(size_t(batch) * 4);
-        pl.off_log = pl.off_map + align256(size_t(batch) * 2 * size_t(n));
-        pl.qwork_bytes = size_t(batch) * size_t(lcap) * sizeof(float2);
-        pl.work_bytes = pl.off_log + pl.qwork_bytes;
-        if (pl.work_bytes < 256)
-            pl.work_bytes = 256;
+        pl.lcap = lay.lcap;
+        pl.off_cnt = lay.off_cnt;
+        pl.off_map = lay.off_map;
+        pl.off_log = lay.off_log;
+        pl.qwork_bytes = lay.total - lay.off_log;
+        pl.work_bytes = lay.total;
         return 0;
     }
     if (qs == QS_SPLIT && (nm == 24 || nm == 32)) {
@@ -859,10 +851,21 @@ extern "C" int bstq_describe(bstq_dtype dtype, bstq_jobz jobz, int n, int64_t ba
             regs = fa.numRegs;
         else
             cudaGetLastError();
-        snprintf(buf, len, "%s<%s,%d,%s,%s,%s> tpb=%d grid=%lld smem=%zu regs=%d work=%zu",
-                 pl.k->family == FAMILY_DYNAMIC ? "dyn" : "lane", dtype ? "f64" : "f32", pl.k->nm,
-                 jobz ? "V" : "N", jobz ? qs_name(pl.k->qs) : "none",
-                 pl.k->sched == SCHED_FLAT ? "flat" : "nested", pl.tpb, pl.grid, pl.smem, regs, pl.work_bytes);
+        int w = snprintf(buf, len, "%s<%s,%d,%s,%s,%s> tpb=%d grid=%lld smem=%zu regs=%d work=%zu",
+                         pl.k->family == FAMILY_DYNAMIC ? "dyn" : "lane", dtype ? "f64" : "f32", pl.k->nm,
+                         jobz ? "V" : "N", jobz ? qs_name(pl.k->qs) : "none",
+                         pl.k->sched == SCHED_FLAT ? "flat" : "nested", pl.tpb, pl.grid, pl.smem, regs,
+                         pl.work_bytes);
+        if (pl.k->qs == QS_LOG && w > 0 && (size_t)w < len) {
+            // the record-and-apply path's other two launches
+            int regs2 = 0;
+            if (cudaFuncGetAttributes(&fa, pl.k->fn2) == cudaSuccess)
+                regs2 = fa.numRegs;
+            else
+                cudaGetLastError();
+            snprintf(buf + w, len - w, " apply: tpb=%d grid=%lld smem=%zu regs=%d; finish: tpb=%d grid=%lld",
+                     pl.tpb2, pl.grid2, pl.smem2, regs2, pl.tpb3, pl.grid3);
+        }
     }
     return 0;
 }

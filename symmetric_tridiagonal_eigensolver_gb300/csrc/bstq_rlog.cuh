@@ -38,13 +38,9 @@
 #include <type_traits>
 
 #include "bstq_dyn.cuh"
+#include "bstq_plan.h"
 
 namespace bstq {
-
-constexpr int kRlogPage = 256;  // log entries per page
-
-// Rows of Q one warp of the apply holds at once (Rlog<NM>::ROWS).
-__host__ __device__ constexpr int rlog_rows(int nm) { return (nm > 32 && nm <= 64) ? 64 : 32; }
 
 template <int NM>
 struct Rlog {

@@ -41,3 +41,36 @@ def test_block_size_matches_the_recorded_launches(tmp_path):
     assert got == [want for _, want in CASES]
     for ((b, s, c, f), (tpb, grid)) in zip([k for k, _ in CASES], got):
         assert tpb % 32 == 0 and tpb <= max(c, 32) and tpb * grid >= b
+
+
+# Record-and-apply layout: (batch, n, n_pad, log_entries) -> (log entries per
+# problem, offsets of the log lengths, maps and logs, total work bytes, apply
+# warps).  The first three totals are the `work=` sizes bstq_describe
+# reported on a GB300 for the bench workloads f32 n = 64 V (batch 32,768),
+# n = 128 V (8,192) and n = 33 V (32,768).
+RLOG_CASES = [
+    ((32768, 64, 64, 0), (6656, 131072, 262144, 4456448, 1749286912, 32768)),
+    ((8192, 128, 128, 0), (25600, 32768, 65536, 2162688, 1679884288, 32768)),
+    ((32768, 33, 48, 0), (2048, 131072, 262144, 2424832, 539295744, 32768)),
+    ((8192, 96, 96, 0), (14592, 32768, 65536, 1638400, 957939712, 24576)),
+    ((300, 40, 48, 1), (256, 1280, 2560, 26624, 641024, 300)),        # one page
+    ((300, 40, 48, 300), (512, 1280, 2560, 26624, 1255424, 300)),     # rounded up to pages
+    ((1, 127, 128, 0), (25344, 256, 512, 768, 203520, 4)),       # 1.5 * 127^2 + 8 * 127 = 25209 -> 99 pages
+]
+
+
+def test_record_and_apply_layout(tmp_path):
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("g++ not available")
+    exe = str(tmp_path / "rlog_layout_check")
+    subprocess.run([gxx, "-std=c++17", "-O1", "-Wall", "-Werror", "-I", CSRC,
+                    os.path.join(ROOT, "tests", "rlog_layout_check.cpp"), "-o", exe], check=True)
+    stdin = "".join(f"{b} {n} {nm} {le}\n" for (b, n, nm, le), _ in RLOG_CASES)
+    r = subprocess.run([exe], input=stdin, capture_output=True, text=True, timeout=60, check=True)
+    got = [tuple(int(x) for x in ln.split()) for ln in r.stdout.splitlines()]
+    assert got == [want for _, want in RLOG_CASES]
+    for (b, n, nm, le), (lcap, oc, om, ol, tot, aw) in zip([k for k, _ in RLOG_CASES], got):
+        assert lcap % 256 == 0 and lcap >= max(le, 1) and lcap >= n + 4
+        assert oc % 256 == 0 and om % 256 == 0 and ol % 256 == 0   # 256-byte aligned regions
+        assert om - oc >= 4 * b and ol - om >= 2 * n * b and tot >= ol + 8 * lcap * b
