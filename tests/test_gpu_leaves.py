@@ -63,7 +63,8 @@ def test_pages_case_float_n64_leaves_of_32(jobz):
 
 @pytest.mark.parametrize("dt,n,leaf,batch", [
     (F64, 64, 32, 2048), (F32, 70, 32, 1000), (F64, 37, 8, 1500), (F32, 130, 16, 300),
-    (F64, 100, 24, 400), (F32, 33, 32, 900), (F64, 12, 5, 2000), (F32, 96, 48, 300), (F64, 128, 64, 120)])
+    (F64, 100, 24, 400), (F32, 33, 32, 900), (F64, 12, 5, 2000), (F32, 96, 48, 300), (F64, 128, 64, 120),
+    (F32, 250, 100, 100)])
 def test_leaf_parity(dt, n, leaf, batch):
     d, e = inputs.normal_problems(n, batch, dt, seed=n + leaf)
     _check(d, e, leaf, jobz=True)
