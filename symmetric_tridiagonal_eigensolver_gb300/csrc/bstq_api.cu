@@ -119,13 +119,14 @@ const KernelEntry *find_entry(int dtype, int jobz, int nm, int qs, int sched, in
 //     problems stays resident);
 //   double: registers for n <= 8, else global scratch (its FP64 pipe, not
 //     L1/L2, bounds it);
-//   float n > 32, flat scheduler: the record-and-apply kernel
-//     (bstq_rlog.cuh); under the nested scheduler the dynamic-position
-//     kernel with Q in global scratch.
+//   float n > 32: the record-and-apply kernels (bstq_rlog.cuh; f32 V n = 64
+//     3.8 against 16.9 ms with Q in global scratch, n = 128 10.7 against
+//     87 ms at batch 8192).
 int default_qstore(int dtype, int nm, int sched)
 {
+    (void)sched;
     if (dtype == 0) {
-        if (nm > 32 && sched == SCHED_FLAT)
+        if (nm > 32)
             return QS_LOG;
         if (nm <= 8)
             return QS_REG;
@@ -158,12 +159,15 @@ int memory_rows(int dtype, int nm, int qs)
 //   double n <= 4, V: nested, on the static-position family (n = 3 0.1024
 //     against 0.1168 for the dynamic family either way, n = 4 0.1751 against
 //     0.2103);
+//   float n > 32, V (the record-and-apply chase, which carries no
+//     eigenvector work): nested (n = 64 3.71 / 3.81 ms, n = 128 at batch
+//     8192 10.16 / 10.75 ms, n = 64 at batch 4096 1.63 / 1.84 ms);
 //   all other sizes: flat (float n = 12 V 0.053 / 0.062, n = 16 V
 //     0.109 / 0.117, n = 32 V 1.95 / 3.39; double within 0.5 %).
 int default_sched(int dtype, int jobz, int nm)
 {
     if (dtype == BSTQ_F32)
-        return (nm <= 4 || (nm <= 8 && !jobz)) ? SCHED_NESTED : SCHED_FLAT;
+        return (nm <= 4 || (nm <= 8 && !jobz) || (nm > 32 && jobz)) ? SCHED_NESTED : SCHED_FLAT;
     return (nm <= 4 && jobz) ? SCHED_NESTED : SCHED_FLAT;
 }
 

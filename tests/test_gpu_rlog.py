@@ -33,9 +33,21 @@ def _describe(n, batch, **params):
 
 def test_default_above_32_is_record_and_apply():
     for n in (33, 64, 65, 128):
-        assert "log" in _describe(n, 4096), n
-    assert "log" not in _describe(64, 4096, scheduler=2)   # nested: the dynamic kernel
+        assert "log" in _describe(n, 4096) and "nested" in _describe(n, 4096), n
+        assert "log" in _describe(n, 4096, scheduler=1), n
+    assert "global" in _describe(64, 4096, qstore=GLOBAL)   # the dynamic-position kernel on request
     assert "log" not in _describe(32, 4096)
+
+
+@pytest.mark.parametrize("n", [40, 64, 128])
+def test_flat_and_nested_chase_agree(n):
+    """The chase's lockstep and per-lane loops run the same operations per
+    problem, so the logs and every output are equal; also when logs run out
+    of room (the finishing launch) and under the PG scheme."""
+    d, e = inputs.normal_problems(n, 700, F32, seed=1200 + n)
+    for kw in ({}, dict(log_entries=1), dict(update_scheme=1)):
+        _same(run_gpu(d, e, qstore=LOG, scheduler=1, **kw), run_gpu(d, e, qstore=LOG, scheduler=2, **kw),
+              f"n={n} {kw}")
 
 
 @pytest.mark.parametrize("n", [33, 40, 47, 48, 57, 63, 64, 65, 80, 96, 101, 127, 128])
@@ -151,7 +163,7 @@ def test_unaligned_q(n):
 def test_rejected_forms():
     from symmetric_tridiagonal_eigensolver_gb300 import bstq
     d, e = inputs.normal_problems(64, 10, F32, seed=1)
-    for kw in (dict(scheduler=2), dict(threads_per_block=1024)):   # 1024 threads: 512 KB of d and e
+    for kw in (dict(threads_per_block=1024),):   # 1024 threads: 512 KB of d and e
         with pytest.raises(bstq.BstqError):
             run_gpu(d, e, qstore=LOG, **kw)
     d, e = inputs.normal_problems(32, 10, F32, seed=1)
