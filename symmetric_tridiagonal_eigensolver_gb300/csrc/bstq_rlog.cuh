@@ -8,13 +8,12 @@
 // applies them afterwards; here that idea spans the whole solve, in three
 // launches:
 //  1. rlog_chase_kernel (either scheduler; nested by default): lane b runs
-//     the dynamic-position chase of problem b
-//     without Q and appends every pass to the problem's rotation log in
-//     global memory: a header (top position m, count L) and the rotations
-//     (cs, sn) of positions m, m-1, ..., m-L+1, the last few of them
-//     identities that end the pass on a multiple of kRlogGroup (bstq_dyn.cuh).
-//     The log is cut into pages
-//     of kRlogPage entries and a pass never crosses a page boundary: a pass
+//     the dynamic-position chase of problem b without Q and appends every
+//     pass to the problem's rotation log in global memory: a header (top
+//     position m, count L) and the rotations (cs, sn) of positions m, m-1,
+//     ..., m-L+1, the last few of them identities that end the pass on a
+//     multiple of kRlogGroup (bstq_dyn.cuh).  The log is cut into pages of
+//     kRlogPage entries and a pass never crosses a page boundary: a pass
 //     that does not fit in the rest of a page starts the next page, after
 //     an end-of-page header (0, 0).  The lane writes the eigenvalues, info,
 //     the log length and the problem's column maps (the initial row of each
@@ -33,7 +32,8 @@
 //     rounds, unpermuted until the last one).
 // Every row of Q sees the same rotations in the same order, with the same
 // arithmetic, as in the dynamic-position kernel; only the order in which
-// the rows are visited changes, so Q is the same to the last bit.
+// the rows are visited changes, so Q is the same to the last bit (the
+// identity padding can only turn a -0 entry into +0).
 #pragma once
 
 #include <type_traits>
@@ -45,8 +45,8 @@ namespace bstq {
 
 template <int NM>
 struct Rlog {
-    // Rows of Q per lane: two for n <= 64 (rows r0 + lane and r0 + 32 +
-    // lane, two independent dependency chains), one above.  Scalar FP32:
+    // Rows of Q per lane: two for 32 < n_pad <= 64 (rows r0 + lane and
+    // r0 + 32 + lane, two independent dependency chains), one otherwise.  Scalar FP32:
     // on GB300 a packed f32x2 rotation (mul, then fma into the other row)
     // measured 23 cycles of latency against 8.4 for the scalar pair, and
     // the update is bound by that chain.
@@ -87,11 +87,11 @@ __device__ __forceinline__ void rlog_rot(float (&q)[RPL][NM], const float2 r)
 // One logged pass: positions m down to lo + 1, lo a multiple of
 // kRlogGroup.  top points at the entry of position 0, so position C's
 // rotation is top[-C].  The switch enters at m; the end test runs only at
-// group boundaries.  An identity rotation leaves the rows as they were
-// (up to the sign of a zero).  Rotations are read two
-// positions ahead into three slots indexed by position mod 3 (compile-time
-// indices, so the slots stay in registers); the reads past the pass's end
-// land in the two slack entries of the page and are not used.
+// group boundaries.  An identity rotation leaves the rows as they were (up
+// to the sign of a zero).  Rotations are read two positions ahead into
+// three slots indexed by position mod 3 (compile-time indices, so the slots
+// stay in registers); the reads past the pass's end land in the two slack
+// entries of the page and are not used.
 template <int NM, int RPL>
 __device__ __forceinline__ void rlog_pass(float (&q)[RPL][NM], const float2 *top, int m, int lo)
 {
