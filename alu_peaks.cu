@@ -4,6 +4,10 @@
 // from unit counts and the maximum clock).  Each thread runs 8 independent
 // FMA chains; the grid is 8 blocks of 256 threads per SM; the best of six
 // timed launches (CUDA events) after two untimed ones is reported.
+// Also the latency of dependent chains, in SM cycles per link (one warp,
+// clock64 around 4,096 links): a scalar FMA, a packed f32x2 FMA, a packed
+// multiply, and one Givens rotation of a row pair (x, y) -> (c x + s y,
+// c y - s x), packed and scalar, whose chain bounds the eigenvector update.
 // Built and run by `python bench.py --alu-peaks`; prints one JSON line.
 #include <cstdint>
 #include <cstdio>
@@ -76,6 +80,81 @@ __global__ void fma_f64(double *out, double b, double c)
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+constexpr int kLinks = 4096;
+
+__device__ __forceinline__ uint64_t pk2(float a, float b)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2v(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2v(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm volatile("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// cyc[0..4]: cycles of kLinks links of each chain (lane 0 of one warp)
+__global__ void chains(float *out, long long *cyc, float cs, float sn)
+{
+    const uint64_t c = pk2(cs, cs), s = pk2(sn, sn), ns = pk2(-sn, -sn);
+    uint64_t x = pk2(threadIdx.x, 1.f), y = pk2(2.f, threadIdx.x * 0.5f);
+    float fx = threadIdx.x, fy = 2.f;
+    long long t0 = clock64();
+    for (int i = 0; i < kLinks; ++i)
+        fx = fmaf(cs, fx, sn);
+    long long t1 = clock64();
+    if (threadIdx.x == 0)
+        cyc[0] = t1 - t0;
+    t0 = clock64();
+    for (int i = 0; i < kLinks; ++i)
+        x = fma2v(c, x, s);
+    t1 = clock64();
+    if (threadIdx.x == 0)
+        cyc[1] = t1 - t0;
+    t0 = clock64();
+    for (int i = 0; i < kLinks; ++i)
+        x = mul2v(c, x);
+    t1 = clock64();
+    if (threadIdx.x == 0)
+        cyc[2] = t1 - t0;
+    t0 = clock64();
+    for (int i = 0; i < kLinks; ++i) {
+        const uint64_t xo = x;
+        x = fma2v(c, x, mul2v(s, y));
+        y = fma2v(c, y, mul2v(ns, xo));
+        const uint64_t t = x;
+        x = y;
+        y = t;
+    }
+    t1 = clock64();
+    if (threadIdx.x == 0)
+        cyc[3] = t1 - t0;
+    t0 = clock64();
+    for (int i = 0; i < kLinks; ++i) {
+        const float xo = fx;
+        fx = fmaf(cs, fx, sn * fy);
+        fy = fmaf(cs, fy, -sn * xo);
+        const float t = fx;
+        fx = fy;
+        fy = t;
+    }
+    t1 = clock64();
+    if (threadIdx.x == 0)
+        cyc[4] = t1 - t0;
+    float a, b, a2, b2;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a2), "=f"(b2) : "l"(y));
+    out[threadIdx.x] = a + b + a2 + b2 + fx + fy;
+}
+
 }  // namespace
 
 int main()
@@ -118,9 +197,21 @@ int main()
         const double fmas = nthreads * kChains * (k == 2 ? kIters / 8 : kIters) * (k == 1 ? 2 : 1);
         tflops[k] = 2.0 * fmas / (best * 1e-3) / 1e12;
     }
+    // dependent-chain latencies: one warp, the last of three launches
+    long long *cyc = nullptr;
+    if (cudaMalloc(&cyc, 5 * sizeof(long long)) != cudaSuccess)
+        return 1;
+    for (int r = 0; r < 3; ++r)
+        chains<<<1, 32>>>(of, cyc, 0.6f, 0.8f);
+    long long hc[5] = {0, 0, 0, 0, 0};
+    if (cudaMemcpy(hc, cyc, sizeof(hc), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return 1;
     printf("{\"fp32_fma_tflops\": %.3f, \"fp32x2_fma_tflops\": %.3f, \"fp64_fma_tflops\": %.4f, "
-           "\"sms\": %d, \"clock_attribute_khz\": %d}\n",
-           tflops[0], tflops[1], tflops[2], sms, clk);
+           "\"sms\": %d, \"clock_attribute_khz\": %d, \"cycles_per_link\": {\"fma\": %.2f, "
+           "\"fma_f32x2\": %.2f, \"mul_f32x2\": %.2f, \"rotation_f32x2\": %.2f, \"rotation_scalar\": %.2f}}\n",
+           tflops[0], tflops[1], tflops[2], sms, clk, hc[0] / (double)kLinks, hc[1] / (double)kLinks,
+           hc[2] / (double)kLinks, hc[3] / (double)kLinks, hc[4] / (double)kLinks);
+    cudaFree(cyc);
     cudaFree(of);
     cudaFree(od);
     return 0;
